@@ -1,0 +1,311 @@
+// (a1) Lightning-indexer scores over the GPU-resident indexer cache.
+//
+// "ESS: Latent-Cache Offload" (foosynaptic tech notes), table "double cache
+// and ESS division of labour": the indexer cache holds one light vector per
+// position and is scored over the whole context every step, so it stays on
+// the GPU.  Score of position s for query way m:
+//     S = fl32( scale_s * sum_h w_h * ReLU(q_h . k_s) ).
+//
+// Persistent, warp-specialised kernel, one CTA per SM:
+//   warp 0     loads the queries of the current request into shared memory
+//              and streams 128-token key tiles (128 B per token) with TMA
+//              into a 6-stage ring;
+//   warp 1     (one lane) issues tcgen05.mma: D[128 tokens][N] = K_tile * Q^T
+//              with e4m3 (kind::f8f6f4) or bf16 (kind::f16) inputs and fp32
+//              accumulators in TMEM, N = ways x heads padded to 32;
+//   warps 2-5  read a token row of D from TMEM per thread, apply ReLU, the
+//              head weights and the key scale, and store the scores.
+// The key tiles are the only large HBM stream; the kernel is bound by HBM
+// bandwidth (about 132 B per token and request).
+#include "ess_device.cuh"
+
+namespace ess {
+namespace {
+
+struct IdxArgs {
+  const float* w;            // [B][M][H_I]
+  const float* scale;        // [B][T] or null (1.0)
+  const int32_t* Tb;         // [B]
+  const int32_t* tile_off;   // [B+1]
+  const uint8_t* q;          // [B][M][H_I][128 B]
+  float* scores;             // [B][M][T]
+  int* status;
+  int B, M, HI, NP, T, total_tiles, A;
+};
+
+constexpr int S = kIdxStages;
+constexpr uint32_t kTileBytes = kIdxTile * kKeyRowBytes;  // 16 KB
+
+__device__ __forceinline__ int find_request(const int32_t* tile_off, int B, int g) {
+  int b = 0;
+  while (b + 1 < B && g >= tile_off[b + 1]) ++b;
+  return b;
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(kIdxThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap kmap, const IdxArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int NP = a.NP;
+  const int A = a.A;
+  uint8_t* kst = smem;                                   // S x 16 KB key tiles
+  uint8_t* qbuf = kst + S * kTileBytes;                  // 2 x NP x 128 B queries
+  float* wbuf = reinterpret_cast<float*>(qbuf + 2 * NP * 128);  // 2 x NP weights
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wbuf + 2 * NP);
+  uint64_t* full = bars;
+  uint64_t* empty = full + S;
+  uint64_t* accf = empty + S;
+  uint64_t* acce = accf + 4;
+  uint64_t* qfull = acce + 4;
+  uint64_t* qempty = qfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* consumed = abort_flag + 1;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  const int g0 = static_cast<int>((static_cast<long long>(blockIdx.x) * a.total_tiles) / gridDim.x);
+  const int g1 =
+      static_cast<int>((static_cast<long long>(blockIdx.x + 1) * a.total_tiles) / gridDim.x);
+  const int MH = a.M * a.HI;
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(smem_u32(&accf[i]), 1);
+      mbar_init(smem_u32(&acce[i]), 128);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&qfull[i]), 1);
+      mbar_init(smem_u32(&qempty[i]), 1 + 128);
+    }
+    *abort_flag = 0;
+    *consumed = 0;
+    fence_mbar_init();
+  }
+  uint32_t ncols = 32;
+  while (ncols < static_cast<uint32_t>(A * NP)) ncols <<= 1;
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), ncols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&kmap);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ producer
+    int b = find_request(a.tile_off, a.B, g0);
+    int cur_b = -1, seg = -1, it = 0;
+    bool ok = true;
+    for (int g = g0; g < g1 && ok; ++g, ++it) {
+      while (b + 1 < a.B && g >= a.tile_off[b + 1]) ++b;
+      const int j = g - a.tile_off[b];
+      if (b != cur_b) {
+        ++seg;
+        const int qb = seg & 1;
+        if (seg >= 2) {
+          int w_ok = 1;
+          if (lane == 0)
+            w_ok = mbar_wait(smem_u32(&qempty[qb]), ((seg >> 1) - 1) & 1, abort_flag) ? 1 : 0;
+          w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+          if (!w_ok) {
+            ok = false;
+            break;
+          }
+        }
+        // queries: NP rows x 128 B, 128B-swizzled, zero rows past M*H_I
+        uint8_t* qd = qbuf + qb * NP * 128;
+        const uint8_t* qs = a.q + static_cast<size_t>(b) * MH * 128;
+        for (int c = lane; c < NP * 8; c += 32) {
+          const int row = c >> 3, ch = c & 7;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (row < MH) v = __ldg(reinterpret_cast<const uint4*>(qs + row * 128 + ch * 16));
+          *reinterpret_cast<uint4*>(qd + sw128_off(row, ch)) = v;
+        }
+        float* wd = wbuf + qb * NP;
+        for (int n = lane; n < NP; n += 32)
+          wd[n] = (n < MH) ? __ldg(a.w + static_cast<size_t>(b) * MH + n) : 0.0f;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&qfull[qb]));
+        cur_b = b;
+      }
+      int w_ok = 1;
+      if (lane == 0) {
+        const int s = it % S;
+        if (it >= S) w_ok = mbar_wait(smem_u32(&empty[s]), ((it / S) - 1) & 1, abort_flag) ? 1 : 0;
+        if (w_ok) {
+          mbar_arrive_expect_tx(smem_u32(&full[s]), kTileBytes);
+          tma_load_2d(smem_u32(kst + s * kTileBytes), &kmap, smem_u32(&full[s]), 0,
+                      b * a.T + j * kIdxTile);
+        }
+      }
+      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+      if (!w_ok) ok = false;
+    }
+    if (!ok) {
+      if (lane == 0) {
+        set_status(a.status, ESS_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+    // drain: wait (bounded) for every issued tile load to land
+    if (lane == 0 && *abort_flag) {
+      for (int i = *consumed; i < it; ++i) mbar_wait(smem_u32(&full[i % S]), (i / S) & 1, nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = FP8 ? make_idesc(kFmtE4M3, kFmtE4M3, 0, NP, 128)
+                                 : make_idesc(kFmtBF16, kFmtBF16, 0, NP, 128);
+      int b = find_request(a.tile_off, a.B, g0);
+      int cur_b = -1, seg = -1, it = 0;
+      for (int g = g0; g < g1; ++g, ++it) {
+        while (b + 1 < a.B && g >= a.tile_off[b + 1]) ++b;
+        if (b != cur_b) {
+          if (seg >= 0) umma_commit(smem_u32(&qempty[seg & 1]));
+          ++seg;
+          if (!mbar_wait(smem_u32(&qfull[seg & 1]), (seg >> 1) & 1, abort_flag)) break;
+          cur_b = b;
+        }
+        const int s = it % S;
+        if (!mbar_wait(smem_u32(&full[s]), (it / S) & 1, abort_flag)) break;
+        *consumed = it + 1;
+        const int acc = it % A;
+        if (it >= A && !mbar_wait(smem_u32(&acce[acc]), ((it / A) - 1) & 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(kst + s * kTileBytes);
+        const uint32_t b_base = smem_u32(qbuf + (seg & 1) * NP * 128);
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * NP);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = make_sdesc_sw128(a_base + kk * 32, 16, 1024);
+          const uint64_t bd = make_sdesc_sw128(b_base + kk * 32, 16, 1024);
+          if (FP8)
+            umma_f8(d, ad, bd, idesc, kk > 0);
+          else
+            umma_f16(d, ad, bd, idesc, kk > 0);
+        }
+        umma_commit(smem_u32(&empty[s]));
+        umma_commit(smem_u32(&accf[acc]));
+      }
+      if (seg >= 0) umma_commit(smem_u32(&qempty[seg & 1]));
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 2..5)
+    const int quad = warp & 3;               // TMEM lanes 32*quad .. +31
+    const int row = quad * 32 + lane;        // token row of the tile
+    int b = find_request(a.tile_off, a.B, g0);
+    int cur_b = -1, seg = -1, it = 0;
+    int Tcur = 0;
+    for (int g = g0; g < g1; ++g, ++it) {
+      while (b + 1 < a.B && g >= a.tile_off[b + 1]) ++b;
+      const int j = g - a.tile_off[b];
+      if (b != cur_b) {
+        ++seg;
+        if (!mbar_wait(smem_u32(&qfull[seg & 1]), (seg >> 1) & 1, abort_flag)) break;
+        cur_b = b;
+        Tcur = a.Tb[b];
+      }
+      const int acc = it % A;
+      if (!mbar_wait(smem_u32(&accf[acc]), (it / A) & 1, abort_flag)) break;
+      tc_fence_after();
+      const float* wq = wbuf + (seg & 1) * NP;
+      float sm[kMaxWays];
+#pragma unroll
+      for (int m = 0; m < kMaxWays; ++m) sm[m] = 0.0f;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                             static_cast<uint32_t>(acc * NP);
+      for (int c = 0; c < NP / 32; ++c) {
+        float v[32];
+        tmem_ld32(taddr + c * 32, v);
+        // columns n = c*32 + i belong to way n / H_I (H_I % 32 == 0 or M == 1)
+        const int m = (a.M == 1) ? 0 : (c * 32) / a.HI;
+        float part = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) part = fmaf(wq[c * 32 + i], fmaxf(v[i], 0.0f), part);
+        // every term is exact under the score contract, so the order is free
+        if (m == 0) sm[0] += part;
+        else if (m == 1) sm[1] += part;
+        else if (m == 2) sm[2] += part;
+        else sm[3] += part;
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&acce[acc]));
+      const int t = j * kIdxTile + row;
+      if (t < Tcur) {
+        const float sc = a.scale ? __ldg(a.scale + static_cast<size_t>(b) * a.T + t) : 1.0f;
+        for (int m = 0; m < a.M; ++m) {
+          const float s = __fmul_rn(sm[m], sc) + 0.0f;  // one rounding; +0 for a zero score
+          a.scores[(static_cast<size_t>(b) * a.M + m) * a.T + t] = s;
+        }
+      }
+      // end of this request's segment: release the query buffer
+      const bool last = (g + 1 == g1) || (g + 1 >= a.tile_off[b + 1]);
+      if (last) mbar_arrive(smem_u32(&qempty[seg & 1]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, ncols);
+  }
+}
+
+size_t indexer_smem_bytes(int NP) {
+  return 1024 + static_cast<size_t>(S) * kTileBytes + 2u * NP * 128 + 2u * NP * 4 +
+         (2 * S + 8 + 4) * 8 + 16;
+}
+
+}  // namespace
+
+cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, const float* w,
+                           float* scores, cudaStream_t st) {
+  const ess_config& c = p.cfg;
+  const Layer& L = p.layers[layer];
+  if (L.total_tiles == 0) return cudaSuccess;
+  IdxArgs a;
+  a.w = w;
+  a.scale = L.idx_scale;
+  a.Tb = L.T_dev;
+  a.tile_off = L.tile_off;
+  a.q = static_cast<const uint8_t*>(q_idx);
+  a.scores = scores;
+  a.status = p.scr.status;
+  a.B = c.batch;
+  a.M = c.mtp;
+  a.HI = c.idx_heads;
+  a.NP = ((c.mtp * c.idx_heads + 31) / 32) * 32;
+  a.T = c.max_T;
+  a.total_tiles = L.total_tiles;
+  a.A = 512 / a.NP < 4 ? 512 / a.NP : 4;
+  const int grid = L.total_tiles < p.num_sms ? L.total_tiles : p.num_sms;
+  const size_t smem = indexer_smem_bytes(a.NP);
+  cudaError_t e;
+  if (c.idx_dtype == ESS_FP8_E4M3) {
+    e = cudaFuncSetAttribute(indexer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    indexer_kernel<true><<<grid, kIdxThreads, smem, st>>>(L.kmap, a);
+  } else {
+    e = cudaFuncSetAttribute(indexer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    indexer_kernel<false><<<grid, kIdxThreads, smem, st>>>(L.kmap, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ess

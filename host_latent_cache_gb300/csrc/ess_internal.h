@@ -1,0 +1,118 @@
+// Internal declarations shared by the host API and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ess.h"
+
+namespace ess {
+
+constexpr int kRowDim = 576;          // D = 512 latent + 64 RoPE (bf16)
+constexpr int kRowBytes = kRowDim * 2;
+constexpr int kLatent = 512;
+constexpr int kMaxWays = 4;
+constexpr int kMaxWayK = 8192;        // M * k cap of the selection lists
+constexpr int kKeyRowBytes = 128;     // one indexer key row
+
+constexpr int kIdxThreads = 192;      // 6 warps: TMA, MMA, 4 epilogue
+constexpr int kIdxStages = 6;         // key-tile ring
+constexpr int kIdxTile = 128;         // tokens per tile (MMA M)
+
+constexpr int kSelCluster = 8;        // CTAs per request in the selection kernel
+constexpr int kSelThreads = 512;
+
+constexpr int kAttnRows = 128;        // selected rows per attention CTA
+constexpr int kAttnThreads = 128;
+constexpr int kAttnQStages = 4;
+
+constexpr int kStatFields = 6;        // ess_stats fields kept on the device
+
+// Bindings and state of one layer (device pointers point into the workspace
+// or at caller buffers).
+struct Layer {
+  bool bound = false;
+  const uint16_t* host_latent = nullptr;  // device-accessible alias of the pinned host rows
+  const int32_t* page_table = nullptr;
+  const uint8_t* idx_keys = nullptr;
+  const float* idx_scale = nullptr;
+  int32_t* T_dev = nullptr;       // [B]
+  int32_t* tile_off = nullptr;    // [B+1] prefix of indexer tiles
+  int32_t total_tiles = 0;
+  int32_t T_hmax = 0;             // max over requests of T_b
+  CUtensorMap kmap;               // keys as [B*T rows][128 B], 128x128 boxes, 128B swizzle
+  // state
+  int32_t* cache_slots = nullptr; // [B][T]
+  int32_t* slot_token = nullptr;  // [B][C]
+  int32_t* last_used = nullptr;   // [B][C]
+  int32_t* step = nullptr;        // [B]
+  uint16_t* pool = nullptr;       // [B][C][D] bf16
+  long long* stats = nullptr;     // [kStatFields]
+};
+
+struct Scratch {
+  float* scores = nullptr;        // [B][M][T]
+  int32_t* topk_idx = nullptr;    // [B][M][k]
+  int32_t* topk_slot = nullptr;   // [B][M][k]
+  int32_t* n_miss_way = nullptr;  // [B][M]
+  int32_t* miss_tok = nullptr;    // [B][M*k]
+  int32_t* miss_slot = nullptr;   // [B][M*k]
+  int32_t* n_miss = nullptr;      // [B]
+  unsigned long long* vict = nullptr;  // [B][M*k]
+  float* part_o = nullptr;        // [B][M][nch][H][512]
+  float2* part_ml = nullptr;      // [B][M][nch][H]
+  uint8_t* h_qidx = nullptr;      // staging for ess_step_host
+  float* h_w = nullptr;
+  uint16_t* h_qmla = nullptr;
+  float* h_out = nullptr;
+  int32_t* status = nullptr;      // device status word
+};
+
+// Workspace layout computed from a config (offsets in bytes).
+struct Layout {
+  size_t total = 0;
+  size_t layer_bytes = 0;
+  // per layer (relative to the layer base)
+  size_t o_T, o_tiles, o_cslots, o_stoken, o_lused, o_step, o_pool, o_stats;
+  // scratch (absolute)
+  size_t o_scores, o_tidx, o_tslot, o_nmw, o_mtok, o_mslot, o_nmiss, o_vict, o_po, o_pml,
+      o_hq, o_hw, o_hqm, o_hout, o_status;
+  int nch = 0;                    // attention chunks per (request, way)
+};
+
+}  // namespace ess
+
+struct ess_pool {
+  ess_config cfg;
+  char* ws = nullptr;
+  size_t ws_bytes = 0;
+  int device = 0;
+  int num_sms = 0;
+  ess::Layout lay;
+  ess::Layer* layers = nullptr;
+  ess::Scratch scr;
+};
+
+namespace ess {
+
+// Kernel launchers (one per kernel file).  They assume validated arguments.
+cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, const float* w,
+                           float* scores, cudaStream_t st);
+cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, int32_t* topk_idx,
+                          int32_t* topk_slot, int32_t* n_miss_way, int32_t* miss_tok,
+                          int32_t* miss_slot, int32_t* n_miss, cudaStream_t st);
+cudaError_t launch_stage(const ess_pool& p, int layer, const int32_t* miss_tok,
+                         const int32_t* miss_slot, const int32_t* n_miss, cudaStream_t st);
+cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
+                             const int32_t* topk_idx, const int32_t* topk_slot, float* out,
+                             bool misses_staged, cudaStream_t st);
+cudaError_t launch_reset(const ess_pool& p, int layer, cudaStream_t st);
+
+// Encodes a 2-D tiled tensor map; returns false on failure.
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                   uint64_t inner_elems, uint64_t outer_rows, uint64_t row_stride_bytes,
+                   uint32_t box_inner, uint32_t box_rows);
+
+}  // namespace ess

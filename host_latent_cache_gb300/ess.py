@@ -1,0 +1,237 @@
+"""Python binding of the C ABI in include/ess.h (argument marshalling only).
+
+Every compute step runs in the CUDA library; this module converts torch
+tensors to pointers and checks status codes.  Importing it needs no GPU;
+loading the library does, and fails loudly when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_lib", "libess.so")
+
+ESS_OK = 0
+ESS_ERR_INVALID_ARG = 1
+ESS_ERR_CAPACITY = 2
+ESS_ERR_UNSUPPORTED = 3
+ESS_ERR_OOM = 4
+ESS_ERR_CUDA = 5
+ESS_ERR_TIMEOUT = 6
+ESS_ERR_DEVICE_CHECK = 7
+
+ESS_FP8_E4M3 = 0
+ESS_BF16 = 1
+ESS_MISS_FUSED = 0
+ESS_MISS_STAGED = 1
+
+# every exported symbol of include/ess.h
+EXPORTS = (
+    "ess_status_string", "ess_pool_device_bytes", "ess_pool_create", "ess_pool_destroy",
+    "ess_pool_bind_layer", "ess_pool_reset", "ess_indexer_scores", "ess_select_manage",
+    "ess_indexer_topk", "ess_stage_misses", "ess_sparse_mla_decode", "ess_step", "ess_step_host",
+    "ess_pipeline_step", "ess_pool_get_state", "ess_pool_set_state", "ess_pool_get_rows",
+    "ess_pool_read_stats", "ess_pool_poll",
+)
+
+
+class ess_config(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32), ("batch", ctypes.c_int32), ("max_T", ctypes.c_int32),
+        ("C", ctypes.c_int32), ("page", ctypes.c_int32), ("k", ctypes.c_int32),
+        ("mtp", ctypes.c_int32), ("idx_heads", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
+        ("idx_dtype", ctypes.c_int32), ("mla_heads", ctypes.c_int32),
+        ("latent_dim", ctypes.c_int32), ("rope_dim", ctypes.c_int32),
+        ("sm_scale", ctypes.c_float), ("miss_mode", ctypes.c_int32),
+    ]
+
+
+class ess_stats(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_int64), ("hits", ctypes.c_int64), ("misses", ctypes.c_int64),
+                ("union_size", ctypes.c_int64), ("miss_rows", ctypes.c_int64),
+                ("miss_bytes", ctypes.c_int64)]
+
+
+class EssError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libess.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    lib.ess_status_string.restype = ctypes.c_char_p
+    lib.ess_status_string.argtypes = [I]
+    sigs = {
+        "ess_pool_device_bytes": [ctypes.POINTER(ess_config), ctypes.POINTER(ctypes.c_size_t)],
+        "ess_pool_create": [ctypes.POINTER(ess_config), P, ctypes.c_size_t, ctypes.POINTER(P)],
+        "ess_pool_destroy": [P],
+        "ess_pool_bind_layer": [P, I, P, P, P, P, P],
+        "ess_pool_reset": [P, I, P],
+        "ess_indexer_scores": [P, I, P, P, P, P],
+        "ess_select_manage": [P, I, P, P, P, P, P, P, P, P],
+        "ess_indexer_topk": [P, I, P, P, P, P, P, P, P, P, P],
+        "ess_stage_misses": [P, I, P, P, P, P],
+        "ess_sparse_mla_decode": [P, I, P, P, P, P, P],
+        "ess_step": [P, I, P, P, P, P, P],
+        "ess_step_host": [P, I, P, P, P, P, P],
+        "ess_pipeline_step": [P, I, I, P, P, P, P, P],
+        "ess_pool_get_state": [P, I, P, P, P, P],
+        "ess_pool_set_state": [P, I, P, P, P, P],
+        "ess_pool_get_rows": [P, I, P],
+        "ess_pool_read_stats": [P, I, ctypes.POINTER(ess_stats), I],
+        "ess_pool_poll": [P, P],
+    }
+    for name, args in sigs.items():
+        f = getattr(lib, name)
+        f.restype = I
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().ess_status_string(code).decode()
+    except Exception:
+        return f"status {code}"
+
+
+def check(code: int, where: str) -> None:
+    if code != ESS_OK:
+        raise EssError(code, where)
+
+
+def _p(t) -> Optional[int]:
+    """Device/host address of a torch tensor (None -> NULL)."""
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_config(*, n_layers, batch, max_T, C, k, mtp, idx_heads, idx_dim, idx_dtype, mla_heads,
+                sm_scale, page=64, miss_mode=ESS_MISS_FUSED, latent_dim=512,
+                rope_dim=64) -> ess_config:
+    return ess_config(n_layers, batch, max_T, C, page, k, mtp, idx_heads, idx_dim, idx_dtype,
+                      mla_heads, latent_dim, rope_dim, float(sm_scale), miss_mode)
+
+
+def ess_pool_device_bytes(cfg: ess_config) -> int:
+    n = ctypes.c_size_t(0)
+    check(load().ess_pool_device_bytes(ctypes.byref(cfg), ctypes.byref(n)), "ess_pool_device_bytes")
+    return n.value
+
+
+def ess_pool_create(cfg: ess_config, workspace) -> int:
+    h = ctypes.c_void_p(0)
+    check(load().ess_pool_create(ctypes.byref(cfg), _p(workspace), workspace.numel() *
+                                 workspace.element_size(), ctypes.byref(h)), "ess_pool_create")
+    return h.value
+
+
+def ess_pool_destroy(pool: int) -> None:
+    check(load().ess_pool_destroy(pool), "ess_pool_destroy")
+
+
+def ess_pool_bind_layer(pool, layer, host_latent, page_table, idx_keys, idx_scale, T_host) -> None:
+    check(load().ess_pool_bind_layer(pool, layer, _p(host_latent), _p(page_table), _p(idx_keys),
+                                     _p(idx_scale), _p(T_host)), "ess_pool_bind_layer")
+
+
+def ess_pool_reset(pool, layer, stream=None) -> None:
+    check(load().ess_pool_reset(pool, layer, _stream(stream)), "ess_pool_reset")
+
+
+def ess_indexer_scores(pool, layer, q_idx, w, scores, stream=None) -> None:
+    check(load().ess_indexer_scores(pool, layer, _p(q_idx), _p(w), _p(scores), _stream(stream)),
+          "ess_indexer_scores")
+
+
+def ess_select_manage(pool, layer, scores, topk_idx, topk_slot, n_miss_way, miss_tok, miss_slot,
+                      n_miss, stream=None) -> None:
+    check(load().ess_select_manage(pool, layer, _p(scores), _p(topk_idx), _p(topk_slot),
+                                   _p(n_miss_way), _p(miss_tok), _p(miss_slot), _p(n_miss),
+                                   _stream(stream)), "ess_select_manage")
+
+
+def ess_indexer_topk(pool, layer, q_idx, w, topk_idx, topk_slot, n_miss_way, miss_tok, miss_slot,
+                     n_miss, stream=None) -> None:
+    check(load().ess_indexer_topk(pool, layer, _p(q_idx), _p(w), _p(topk_idx), _p(topk_slot),
+                                  _p(n_miss_way), _p(miss_tok), _p(miss_slot), _p(n_miss),
+                                  _stream(stream)), "ess_indexer_topk")
+
+
+def ess_stage_misses(pool, layer, miss_tok, miss_slot, n_miss, stream=None) -> None:
+    check(load().ess_stage_misses(pool, layer, _p(miss_tok), _p(miss_slot), _p(n_miss),
+                                  _stream(stream)), "ess_stage_misses")
+
+
+def ess_sparse_mla_decode(pool, layer, q_mla, topk_idx, topk_slot, out, stream=None) -> None:
+    check(load().ess_sparse_mla_decode(pool, layer, _p(q_mla), _p(topk_idx), _p(topk_slot),
+                                       _p(out), _stream(stream)), "ess_sparse_mla_decode")
+
+
+def ess_step(pool, layer, q_idx, w, q_mla, out, stream=None) -> None:
+    check(load().ess_step(pool, layer, _p(q_idx), _p(w), _p(q_mla), _p(out), _stream(stream)),
+          "ess_step")
+
+
+def ess_step_host(pool, layer, q_idx, w, q_mla, out, stream=None) -> None:
+    check(load().ess_step_host(pool, layer, _p(q_idx), _p(w), _p(q_mla), _p(out),
+                               _stream(stream)), "ess_step_host")
+
+
+def ess_pipeline_step(pools: Sequence[int], n_layers: int, q_idx, w, q_mla, out, streams) -> None:
+    n = len(pools)
+    arr = lambda xs, T=ctypes.c_void_p: (T * len(xs))(*xs)
+    check(load().ess_pipeline_step(arr(list(pools)), n, n_layers, arr([_p(x) for x in q_idx]),
+                                   arr([_p(x) for x in w]), arr([_p(x) for x in q_mla]),
+                                   arr([_p(x) for x in out]), arr([_stream(s) for s in streams])),
+          "ess_pipeline_step")
+
+
+def ess_pool_get_state(pool, layer, cache_slots, slot_token, last_used, step) -> None:
+    check(load().ess_pool_get_state(pool, layer, _p(cache_slots), _p(slot_token), _p(last_used),
+                                    _p(step)), "ess_pool_get_state")
+
+
+def ess_pool_set_state(pool, layer, cache_slots, slot_token, last_used, step) -> None:
+    check(load().ess_pool_set_state(pool, layer, _p(cache_slots), _p(slot_token), _p(last_used),
+                                    _p(step)), "ess_pool_set_state")
+
+
+def ess_pool_get_rows(pool, layer, rows_host) -> None:
+    check(load().ess_pool_get_rows(pool, layer, _p(rows_host)), "ess_pool_get_rows")
+
+
+def ess_pool_read_stats(pool, layer, reset: bool = False) -> ess_stats:
+    s = ess_stats()
+    check(load().ess_pool_read_stats(pool, layer, ctypes.byref(s), int(reset)), "ess_pool_read_stats")
+    return s
+
+
+def ess_pool_poll(pool, stream=None) -> int:
+    return load().ess_pool_poll(pool, _stream(stream))

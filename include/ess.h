@@ -1,0 +1,254 @@
+/*
+ * ess.h - C ABI of the GB300 sparse-decode library with a host-resident
+ * MLA latent cache.
+ *
+ * One decode layer of DSA-style sparse attention whose latent cache lives
+ * in pinned host memory:
+ *   (a1) lightning-indexer scores over the GPU-resident indexer cache,
+ *   (a2) exact top-k, (a3) hit/miss resolution against the token->slot
+ *   reverse index cache_slots and the miss union over MTP ways, (a4) LRU
+ *   victim choice and state rewrite with copy triples, (a5) sparse
+ *   absorbed-MLA attention whose row gather forks per row: hits from the
+ *   HBM hot pool, misses straight from pinned host memory, (a6) a separate
+ *   miss-staging copy, and per-step counters.
+ *
+ * Sources (web pages on latent-cache offload for DSA sparse decode):
+ *   [FO]  hwcomputing.csdn.net, analysis of FlashOffloading
+ *         - "decode side (1)": cache_slots, the five-step steady-state flow,
+ *           the MTP3 miss union, LIM and its worked example (Figure 4);
+ *         - "decode side (2)": CopySFA, the gather that forks on hit/miss;
+ *         - "architecture": one host master copy, paged by request, layer
+ *           and token block behind a block table; a hot cache of C slots.
+ *   [ESS] foosynaptic tech notes, "ESS: Latent-Cache Offload": the indexer
+ *         cache stays on the GPU and scores every position; the latent
+ *         entry is c^KV[512] + k^R[64]; a GPU sparse pool under LRU.
+ *   [DEP] cloud.baidu.com deployment article, "monitoring": hit rate and
+ *         link utilisation counters.
+ *
+ * Conventions for every call:
+ *   - Device pointers are CUDA device addresses; "pinned host" pointers come
+ *     from cudaHostAlloc / cudaHostRegister and stay valid while bound.
+ *   - The caller owns every buffer it passes, including the device
+ *     workspace given to ess_pool_create.  The library owns only the opaque
+ *     handle and never calls cudaMalloc.
+ *   - Calls that take a stream are asynchronous on that stream.  Errors the
+ *     host can detect are returned at once and nothing is launched.  Errors
+ *     found on the device (bounds checks, capacity, a wait that timed out)
+ *     are recorded in a device status word and returned by ess_pool_poll.
+ *     No kernel traps or asserts.
+ *   - A pool is not thread-safe.  Calls on one pool must be ordered on one
+ *     stream (or ordered by the caller with events); they share scratch.
+ *   - Layouts are row-major, the last index fastest.  B = batch, M = MTP
+ *     ways, T = max_T, k = top-k, C = hot-pool slots per request, H_I =
+ *     indexer heads, H = MLA heads, D = latent_dim + rope_dim = 576.
+ */
+#ifndef ESS_H
+#define ESS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ess_pool ess_pool;
+/* A cudaStream_t passed as an opaque pointer (NULL = the legacy stream). */
+typedef void* ess_stream_t;
+
+typedef enum {
+  ESS_OK = 0,
+  ESS_ERR_INVALID_ARG = 1,   /* bad pointer, size, layer or layout            */
+  ESS_ERR_CAPACITY = 2,      /* the miss union cannot fit the C slots        */
+  ESS_ERR_UNSUPPORTED = 3,   /* shape/dtype outside what the kernels handle  */
+  ESS_ERR_OOM = 4,           /* the workspace is smaller than required       */
+  ESS_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed            */
+  ESS_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up           */
+  ESS_ERR_DEVICE_CHECK = 7   /* a device-side bounds check failed            */
+} ess_status;
+
+enum { ESS_FP8_E4M3 = 0, ESS_BF16 = 1 };
+/* FUSED: the attention kernel reads misses from host memory and writes them
+ * to their pool slot in the same pass ([FO] "decode side (2)", CopySFA).
+ * STAGED: a separate copy kernel moves the misses first ([FO] "decode side
+ * (1)", step 5), then attention reads every row from the pool. */
+enum { ESS_MISS_FUSED = 0, ESS_MISS_STAGED = 1 };
+
+typedef struct {
+  int32_t n_layers;    /* layers held by this pool                            */
+  int32_t batch;       /* B requests                                          */
+  int32_t max_T;       /* T: context capacity per request, a multiple of page */
+  int32_t C;           /* hot-pool slots per request and layer ([FO] C_b)     */
+  int32_t page;        /* host page size in tokens (block-table granularity)  */
+  int32_t k;           /* top-k per way ([FO]: k = 2048)                      */
+  int32_t mtp;         /* M ways per step, 1..4 ([FO]: MTP3 = 4 ways)         */
+  int32_t idx_heads;   /* H_I                                                 */
+  int32_t idx_dim;     /* d_I; a key row must be 128 bytes                    */
+  int32_t idx_dtype;   /* ESS_FP8_E4M3 (d_I = 128) or ESS_BF16 (d_I = 64)     */
+  int32_t mla_heads;   /* H, 1..128                                           */
+  int32_t latent_dim;  /* 512 ([ESS]: c^KV[512])                              */
+  int32_t rope_dim;    /* 64  ([ESS]: k^R)                                    */
+  float sm_scale;      /* softmax scale applied to q . row                   */
+  int32_t miss_mode;   /* ESS_MISS_FUSED or ESS_MISS_STAGED                   */
+} ess_config;
+
+/* Counters accumulated per layer since the last read with reset ([DEP]
+ * "monitoring": hit rate and link traffic). */
+typedef struct {
+  int64_t steps;        /* decode steps run on the layer (per request)     */
+  int64_t hits;         /* selected rows found in the pool, summed over ways */
+  int64_t misses;       /* selected rows not resident, summed over ways    */
+  int64_t union_size;   /* |U|: distinct rows selected by any way          */
+  int64_t miss_rows;    /* |Miss|: distinct rows moved from host           */
+  int64_t miss_bytes;   /* miss_rows * D * 2                               */
+} ess_stats;
+
+/* Human-readable name of a status code (static storage). */
+const char* ess_status_string(ess_status s);
+
+/* Bytes of device workspace that ess_pool_create needs for cfg.
+ * Covers, per layer: cache_slots [B][T] int32, slot_token [B][C] int32,
+ * last_used [B][C] int32, step [B] int32, the hot pool [B][C][D] bf16 and
+ * counters; plus scratch shared by the layers (scores, selection lists,
+ * attention partials, staging for ess_step_host).
+ * Errors: ESS_ERR_INVALID_ARG / ESS_ERR_UNSUPPORTED for a bad cfg. */
+ess_status ess_pool_device_bytes(const ess_config* cfg, size_t* bytes);
+
+/* Create a pool on the current CUDA device inside a caller-owned device
+ * workspace (at least ess_pool_device_bytes, 256-byte aligned).  Every layer
+ * starts empty (cache_slots = -1, slot_token = -1, last_used = -1, step 0):
+ * the first step fills the pool from host memory ([FO] "decode side (1)",
+ * first fill).  Initialisation is synchronous.  Requires
+ * C >= min(mtp * k, max_T) so the miss union always fits. */
+ess_status ess_pool_create(const ess_config* cfg, void* dev_workspace, size_t ws_bytes,
+                           ess_pool** out);
+
+/* Release the handle (the caller frees the workspace). */
+ess_status ess_pool_destroy(ess_pool* pool);
+
+/* Bind the inputs of one layer ([FO] "architecture": host master copy
+ * behind a block table; [ESS]: indexer cache resident on the GPU).
+ *   host_latent  pinned host, [B][T][D] bf16, physical rows: logical token t
+ *                of request b is row page_table[b][t / page] * page + t % page
+ *   page_table   device int32 [B][T / page], or NULL for the identity map
+ *   idx_keys     device [B][T][128 bytes]: e4m3 keys (d_I = 128) or bf16
+ *                keys (d_I = 64)
+ *   idx_scale    device float [B][T] per-token key scale, or NULL for 1.0
+ *   T_host       host int32 [B], tokens per request, 0 <= T_b <= max_T
+ * Buffers must stay valid and unchanged while the layer is used. */
+ess_status ess_pool_bind_layer(ess_pool* pool, int layer, const void* host_latent,
+                               const int32_t* page_table, const void* idx_keys,
+                               const float* idx_scale, const int32_t* T_host);
+
+/* Empty the hot pool of a layer again (asynchronous on stream). */
+ess_status ess_pool_reset(ess_pool* pool, int layer, ess_stream_t stream);
+
+/* (a1) Indexer scores ([ESS]: score all positions; formula
+ * S[b][m][t] = fl32(scale[b][t] * sum_h w[b][m][h] * ReLU(q[b][m][h] . k[b][t]))).
+ *   q_idx   device [B][M][H_I][128 bytes] (same encoding as the keys)
+ *   w       device float [B][M][H_I]
+ *   scores  device float [B][M][T]; entries t >= T_b are not written */
+ess_status ess_indexer_scores(ess_pool* pool, int layer, const void* q_idx, const float* w,
+                              float* scores, ess_stream_t stream);
+
+/* (a2)-(a4), (a8) Top-k, resolve, miss union and LRU update from given
+ * scores ([FO] "decode side (1)", five-step flow and LIM outputs).
+ *   scores      device float [B][M][T]
+ * Outputs (device):
+ *   topk_idx    int32 [B][M][k]: per way the min(k, T_b) selected tokens,
+ *               misses first (ascending token), then hits (ascending token)
+ *   topk_slot   int32 [B][M][k]: the slot of a hit, or ~slot (= -1 - slot)
+ *               for a miss, naming the slot it is loaded into
+ *   n_miss_way  int32 [B][M]: how many leading entries of way m are misses
+ *   miss_tok    int32 [B][M*k]: the miss union Miss_b, ascending
+ *   miss_slot   int32 [B][M*k]: the paired slot of each miss (copy triple:
+ *               host row of miss_tok -> pool slot miss_slot, one row each)
+ *   n_miss      int32 [B]: |Miss_b|
+ * State: cache_slots, slot_token, last_used and step of the layer are
+ * updated; entries past the selected count are left untouched. */
+ess_status ess_select_manage(ess_pool* pool, int layer, const float* scores,
+                             int32_t* topk_idx, int32_t* topk_slot, int32_t* n_miss_way,
+                             int32_t* miss_tok, int32_t* miss_slot, int32_t* n_miss,
+                             ess_stream_t stream);
+
+/* (a1)-(a4) ess_indexer_scores followed by ess_select_manage, with the
+ * scores kept in the pool's scratch ([FO] LIM: LI plus management).
+ * Output arguments as in ess_select_manage. */
+ess_status ess_indexer_topk(ess_pool* pool, int layer, const void* q_idx, const float* w,
+                            int32_t* topk_idx, int32_t* topk_slot, int32_t* n_miss_way,
+                            int32_t* miss_tok, int32_t* miss_slot, int32_t* n_miss,
+                            ess_stream_t stream);
+
+/* (a6) Copy the miss rows host -> pool slots ([FO] "decode side (1)", step
+ * 5): for i < n_miss[b], host row of miss_tok[b][i] -> slot miss_slot[b][i].
+ * Inputs are the device outputs of ess_select_manage. */
+ess_status ess_stage_misses(ess_pool* pool, int layer, const int32_t* miss_tok,
+                            const int32_t* miss_slot, const int32_t* n_miss,
+                            ess_stream_t stream);
+
+/* (a5) Sparse absorbed-MLA attention over the selected rows ([FO] "decode
+ * side (2)": SFA/CopySFA; [ESS]: c^KV[512] + k^R[64]).
+ *   q_mla      device bf16 [B][M][H][D]
+ *   topk_idx, topk_slot: as produced by ess_select_manage
+ *   out        device float [B][M][H][latent_dim]:
+ *              softmax_s(sm_scale * q . row_s) @ row_s[:latent_dim]; zeros
+ *              when nothing is selected
+ * In FUSED mode a row with topk_slot < 0 is read from host memory and also
+ * written to slot ~topk_slot; in STAGED mode every row is read from the pool
+ * (run ess_stage_misses first). */
+ess_status ess_sparse_mla_decode(ess_pool* pool, int layer, const void* q_mla,
+                                 const int32_t* topk_idx, const int32_t* topk_slot, float* out,
+                                 ess_stream_t stream);
+
+/* (a1)-(a6) One decode step of one layer with every intermediate in the
+ * pool's scratch: indexer, selection and management, (staging,) attention.
+ *   q_idx, w  as in ess_indexer_scores;  q_mla, out as in
+ *   ess_sparse_mla_decode. */
+ess_status ess_step(ess_pool* pool, int layer, const void* q_idx, const float* w,
+                    const void* q_mla, float* out, ess_stream_t stream);
+
+/* ess_step with HOST inputs and output: the inputs are copied to device
+ * staging, the step runs, and out is copied back, all on stream (pass pinned
+ * host buffers for asynchronous copies).  Same layouts as ess_step. */
+ess_status ess_step_host(ess_pool* pool, int layer, const void* q_idx_host,
+                         const float* w_host, const void* q_mla_host, float* out_host,
+                         ess_stream_t stream);
+
+/* (a7) Layer-wise pipeline over two micro-batches (two pools with the same
+ * config, e.g. the two halves of a batch): for layer l = 0..n_layers-1 each
+ * pool runs ess_step on its own stream, so one micro-batch's selection and
+ * staging overlap the other's attention ([ESS] layer-wise overlap).
+ * Per-layer arrays are indexed [pool * n_layers + layer]. */
+ess_status ess_pipeline_step(ess_pool* const* pools, int n_pools, int n_layers,
+                             const void* const* q_idx, const float* const* w,
+                             const void* const* q_mla, float* const* out,
+                             const ess_stream_t* streams);
+
+/* Copy the bookkeeping of one layer to host buffers (synchronous):
+ * cache_slots [B][T], slot_token [B][C], last_used [B][C] int32, step [B]. */
+ess_status ess_pool_get_state(ess_pool* pool, int layer, int32_t* cache_slots,
+                              int32_t* slot_token, int32_t* last_used, int32_t* step);
+
+/* Overwrite the bookkeeping of one layer from host buffers (synchronous).
+ * The caller keeps it consistent (cache_slots and slot_token inverse maps)
+ * and the pool rows of resident tokens filled. */
+ess_status ess_pool_set_state(ess_pool* pool, int layer, const int32_t* cache_slots,
+                              const int32_t* slot_token, const int32_t* last_used,
+                              const int32_t* step);
+
+/* Copy the hot pool of one layer, [B][C][D] bf16, to a host buffer
+ * (synchronous); rows of empty slots hold whatever was last written. */
+ess_status ess_pool_get_rows(ess_pool* pool, int layer, void* rows_host);
+
+/* Read (and optionally zero) the per-layer counters (synchronous). */
+ess_status ess_pool_read_stats(ess_pool* pool, int layer, ess_stats* out, int reset);
+
+/* Synchronise stream, return the first device-side error since the last
+ * poll (ESS_OK if none) and clear it. */
+ess_status ess_pool_poll(ess_pool* pool, ess_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ESS_H */
