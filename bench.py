@@ -1,0 +1,359 @@
+"""Benchmark of one sparse-decode layer with a host-resident latent cache.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload long_128k|...] [--miss-mode fused|staged]
+
+A step is one decode step of the layer for the whole batch: indexer scores
+over the GPU-resident indexer cache, exact top-k + cache_slots resolve +
+miss union + LRU update, and sparse MLA attention whose gather reads hits
+from the HBM pool and misses from pinned host memory.  The workload is the
+long-context layer: 8 requests x 131072 tokens, top-2048, 128 MLA heads,
+64x128 e4m3 indexer, hot pool of 32768 slots, query drift rho = 0.9 with 5%
+cold-miss bursts.  Inputs are seeded synthetic data; the keys read per step
+(138 MB) exceed the 129 MB L2, so no flush is inserted between steps.
+
+One JSON line is printed by rank 0.  --impl reference times the CPU oracle
+(float64 numpy) on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+_CORES = os.cpu_count() or 1
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from host_latent_cache_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode token·layers/s at 128K,k=2048; HBM & host-link GB/s vs roofline"
+UNIT = "token·layers/s"
+IDX_BYTES_PER_TOKEN = 128 + 4       # e4m3 key row + fp32 scale, read once per request
+ROW_BYTES = 1152
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=32)
+    ap.add_argument("--warmup", type=int, default=4)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_128k", choices=sorted(W.ALL_CONFIGS))
+    ap.add_argument("--miss-mode", default="fused", choices=["fused", "staged"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-steps", type=int, default=16)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def config_json(cfg: W.WorkloadConfig, n_gpus: int, miss_mode: str):
+    return {
+        "workload": f"{cfg.name}: batch {cfg.batch} x T={cfg.T}, top-k {cfg.k}, "
+                    f"{cfg.mla_heads} MLA heads (512+64 bf16), indexer {cfg.idx_heads}x"
+                    f"{cfg.idx_dim} {'e4m3' if cfg.idx_dtype == W.FP8_E4M3 else 'bf16'}, "
+                    f"C={cfg.C}, MTP={cfg.mtp}, rho={cfg.rho}, cold bursts {cfg.cold_p}",
+        "batch_per_gpu": cfg.batch, "T": cfg.T, "k": cfg.k, "C": cfg.C, "mtp": cfg.mtp,
+        "layers": cfg.layers, "miss_mode": miss_mode,
+        "l2": "inputs larger than L2 (keys read per step exceed the 129 MB L2); no flush",
+        "parallelism": f"replicas x{n_gpus} (independent requests per GPU, no collective)",
+    }
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            p = [x.strip() for x in l.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                sm.append(float(p[0]))
+                smax = float(p[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+def run_oracle(cfg: W.WorkloadConfig, ld: W.LayerData, n_steps: int, n_req: int,
+               warm: int = 1):
+    """Times the CPU oracle on the first n_req requests for n_steps steps
+    (after `warm` untimed steps).  Returns (token.layers/s, seconds)."""
+    from oracle import ess_oracle as O
+    sub = cfg.replace(batch=n_req)
+    keys = W.decode_keys(cfg, ld.idx_keys[:n_req]).astype(np.float32)
+    lay = O.OracleLayer(ld.T[:n_req], cfg.C, cfg.k, cfg.sm_scale)
+    qs = W.QueryStream(sub)
+    keyf = lambda b: keys[b, : int(ld.T[b])]
+    latf = lambda b, order: W.bf16_bits_to_float(ld.latent[b, order]).astype(np.float64)
+    w = W.head_weights(sub, ld.w[:n_req]).astype(np.float64)
+    t = 0.0
+    for s in range(warm + n_steps):
+        q, _, qm = qs.next()
+        qmf = W.bf16_bits_to_float(qm).astype(np.float64)
+        t0 = time.perf_counter()
+        lay.step(q.astype(np.float64), w, keyf, ld.idx_scale, qmf, latf)
+        if s >= warm:
+            t += time.perf_counter() - t0
+    units = n_req * cfg.mtp * cfg.layers * n_steps
+    return units / t, t
+
+
+# ---------------------------------------------------------------- reference arm
+def bench_reference(args, cfg, rank, world):
+    if rank != 0:
+        return 0
+    ld = W.gen_layer(cfg)
+    steps = max(1, args.steps)
+    # a bounded sample per step: all requests while that keeps the run to a few
+    # minutes, fewer requests otherwise
+    n_req = max(1, min(cfg.batch, (cfg.batch * 32) // max(steps, 1)))
+    v, t = run_oracle(cfg, ld, steps, n_req, warm=max(1, min(args.warmup, 2)))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": config_json(cfg, args.gpus, args.miss_mode),
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": _CORES, "kind": "oracle",
+                         "sample": f"{n_req} of {cfg.batch} requests per step, {steps} steps "
+                                   f"after warm-up, float64 numpy with {_CORES} BLAS threads"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def bench_ours(args, cfg, rank, world, local_rank):
+    import torch
+    from host_latent_cache_gb300 import build as B
+    from host_latent_cache_gb300 import ess
+    from host_latent_cache_gb300.session import Session
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if rank == 0:
+        B.build()
+    if dist is not None:
+        dist.barrier()
+    ess.load()
+    # each rank serves its own independent requests (weak scaling)
+    cfg_r = cfg.replace(seed=cfg.seed + 7919 * rank)
+    ld = W.gen_layer(cfg_r)
+    mode = ess.ESS_MISS_STAGED if args.miss_mode == "staged" else ess.ESS_MISS_FUSED
+    sess = Session(cfg_r, [ld], miss_mode=mode)
+    qs = W.QueryStream(cfg_r)
+    n_total = args.warmup + 2 * args.steps
+    wts = W.head_weights(cfg_r, ld.w)
+    dev_inputs, host_inputs = [], []
+    for s in range(n_total):
+        q, enc, qm = qs.next()
+        if s < args.warmup + args.steps:
+            dev_inputs.append(sess.device_inputs(enc, wts, qm))
+        else:
+            hq = torch.from_numpy(np.ascontiguousarray(enc).view(np.uint8)).pin_memory()
+            hw = torch.from_numpy(wts).pin_memory()
+            hqm = torch.from_numpy(np.ascontiguousarray(qm).view(np.int16)).pin_memory()
+            host_inputs.append((hq, hw, hqm))
+    out_host = torch.empty(tuple(sess.out.shape), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    nsteps = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nsteps)]
+    staged = mode == ess.ESS_MISS_STAGED
+
+    def one_step(i, events=None):
+        qd, wd, qmd = dev_inputs[i]
+        if events:
+            events[0].record(stream)
+        sess.scores_only(0, qd, wd, stream)
+        if events:
+            events[1].record(stream)
+        sess.select(0, sess.scores, stream)
+        if staged:
+            sess.stage(0, stream)
+        if events:
+            events[2].record(stream)
+        sess.attention(0, qmd, stream=stream)
+        if events:
+            events[3].record(stream)
+
+    for i in range(args.warmup):
+        one_step(i)
+    torch.cuda.synchronize()
+    assert sess.poll(stream) == ess.ESS_OK
+    sess.stats(0, reset=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        t_start.record(stream)
+        for i in range(nsteps):
+            one_step(args.warmup + i, ev[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    st = sess.poll(stream)
+    assert st == ess.ESS_OK, ess.status_string(st)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    idx_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    sel_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    att_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    stats = sess.stats(0, reset=True)
+
+    # end to end through the public C ABI with host buffers
+    torch.cuda.synchronize()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for i in range(nsteps):
+        hq, hw, hqm = host_inputs[i]
+        ess.ess_step_host(sess.pool, 0, hq, hw, hqm, out_host, stream)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    assert sess.poll(stream) == ess.ESS_OK
+    e2e_ms = e_start.elapsed_time(e_end)
+
+    t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+    units_step = cfg.batch * cfg.mtp * cfg.layers
+    value = world * units_step * nsteps / (elapsed_ms / 1e3)
+    e2e_value = world * units_step * nsteps / (e2e_ms / 1e3)
+
+    result = None
+    if rank == 0:
+        peaks = {}
+        try:
+            peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        except Exception:
+            pass
+        hbm_peak = peaks.get("hbm_gbs")
+        peak_src = "measured" if hbm_peak else "fallback"
+        hbm_peak = hbm_peak or 6800.0
+        Tsum = int(ld.T.sum())
+        idx_bytes = Tsum * IDX_BYTES_PER_TOKEN
+        idx_avg_ms = statistics.mean(idx_ms)
+        achieved = idx_bytes / (idx_avg_ms / 1e3) / 1e9
+        miss_rows = stats.miss_rows / max(nsteps, 1)
+        hit_rows = (stats.hits) / max(nsteps, 1)
+        r_idx_us = idx_bytes / (hbm_peak * 1e9) * 1e6
+        r_hit_us = hit_rows * ROW_BYTES / (hbm_peak * 1e9) * 1e6
+        step_us = elapsed_ms * 1e3 / nsteps
+        traffic = None
+        tr_path = os.path.join(ROOT, "profiles", "indexer_traffic.json")
+        if os.path.exists(tr_path):
+            try:
+                traffic = json.load(open(tr_path)).get("dram_bytes_per_launch")
+            except Exception:
+                traffic = None
+        result = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": nsteps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / nsteps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
+            "config": config_json(cfg, world, args.miss_mode),
+            "roofline": {"bound": "hbm", "kernel": "indexer (a1)", "achieved": achieved,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                         "traffic": traffic, "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": idx_bytes},
+            "layer_roofline": {"R_us": max(r_idx_us, r_hit_us), "step_us": step_us,
+                               "frac": max(r_idx_us, r_hit_us) / step_us,
+                               "terms_us": {"indexer": r_idx_us, "hits": r_hit_us},
+                               "miss_rows_per_step": miss_rows,
+                               "miss_bytes_per_step": miss_rows * ROW_BYTES},
+            "kernels_ms": {"indexer": statistics.mean(idx_ms), "select": statistics.mean(sel_ms),
+                           "attention": statistics.mean(att_ms)},
+            "hit_rate": stats.hits / max(stats.hits + stats.misses, 1),
+            "e2e": {"value": e2e_value, "unit": UNIT,
+                    "h2d_bytes_per_step": int(sum(x.numel() * x.element_size()
+                                                  for x in host_inputs[0])),
+                    "d2h_bytes_per_step": int(out_host.numel() * 4)},
+            "gpu_launches": nsteps * (5 if staged else 4),
+            "clocks": clk.summary(),
+        }
+    sess.close()
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result, ld
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    cfg = W.ALL_CONFIGS[args.workload]()
+    if args.impl == "reference":
+        return bench_reference(args, cfg, rank, world)
+    result, ld = bench_ours(args, cfg, rank, world, local_rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            n_req = min(cfg.batch, 8)
+            v, t = run_oracle(cfg, ld, max(1, args.cpu_steps), n_req)
+            result["cpu_baseline"] = {
+                "value": v, "unit": UNIT, "cores": _CORES, "kind": "oracle",
+                "sample": f"{n_req} requests x {args.cpu_steps} steps of the same workload "
+                          f"after one warm-up step ({t:.1f} s), float64 numpy, "
+                          f"{_CORES} BLAS threads"}
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -217,6 +217,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         cur_b = b;
         Tcur = a.Tb[b];
       }
+      // issue the scale load before waiting so its latency hides under the wait
+      const int t = j * kIdxTile + row;
+      const bool in_range = t < Tcur;
+      float sc = 1.0f;
+      if (a.scale != nullptr && in_range) sc = __ldg(a.scale + static_cast<size_t>(b) * a.T + t);
       const int acc = it % A;
       if (!mbar_wait(smem_u32(&accf[acc]), (it / A) & 1, abort_flag)) break;
       tc_fence_after();
@@ -242,9 +247,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&acce[acc]));
-      const int t = j * kIdxTile + row;
-      if (t < Tcur) {
-        const float sc = a.scale ? __ldg(a.scale + static_cast<size_t>(b) * a.T + t) : 1.0f;
+      if (in_range) {
         for (int m = 0; m < a.M; ++m) {
           const float s = __fmul_rn(sm[m], sc) + 0.0f;  // one rounding; +0 for a zero score
           a.scores[(static_cast<size_t>(b) * a.M + m) * a.T + t] = s;

@@ -31,10 +31,14 @@ Every dot product is then a multiple of 2^-6 below 2^12 in magnitude and
 every weighted ReLU term a non-negative multiple of 2^-12, so all partial
 sums are exact in fp32 in any order while the total stays below 4096.
 
-Query drift follows the workload text literally: per head,
-q_t = normalize(rho * q_{t-1} + (1 - rho) * g) with g ~ N(0, I) drawn per
-element; the normalised fp32 state carries over; each step's query is
-then scaled so that its largest magnitude is 2 and rounded to the grid.
+Query drift: per head, q_t = normalize(rho * q_{t-1} + (1 - rho) * g),
+where the state q is a unit vector and g is isotropic Gaussian noise on the
+same scale, i.e. unit expected norm (per-element variance 1/d).  Read with
+per-element variance 1, the noise would outweigh the unit-norm state ten to
+one in 128 dims and adjacent top-2048 sets would overlap by only about a
+third, against the stated intent of a high adjacent-step overlap.  The
+normalised fp32 state carries over; each step's query is then scaled so
+that its largest magnitude is 2 and rounded to the grid.
 """
 from __future__ import annotations
 
@@ -329,7 +333,7 @@ class QueryStream:
         for b in range(B):
             r = self._rng[b]
             if self.step > 0:
-                g = r.standard_normal((H, d), dtype=np.float32)
+                g = r.standard_normal((H, d), dtype=np.float32) * np.float32(1.0 / np.sqrt(d))
                 cold = cfg.cold_p > 0 and self._cold[b].random() < cfg.cold_p
                 if cold:
                     self.state[b] = self._normalize(g)
@@ -337,7 +341,7 @@ class QueryStream:
                     self.state[b] = self._normalize(rho * self.state[b] + (np.float32(1) - rho) * g)
             ways = [self.state[b]]
             for m in range(1, M):
-                g = r.standard_normal((H, d), dtype=np.float32)
+                g = r.standard_normal((H, d), dtype=np.float32) * np.float32(1.0 / np.sqrt(d))
                 ways.append(self._normalize(rho * ways[-1] + (np.float32(1) - rho) * g))
             for m in range(M):
                 q[b, m] = self._to_grid(ways[m])
