@@ -52,7 +52,8 @@ def parse():
     ap.add_argument("--workload", default="long_128k", choices=sorted(W.ALL_CONFIGS))
     ap.add_argument("--miss-mode", default="fused", choices=["fused", "staged"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-steps", type=int, default=16)
+    ap.add_argument("--cpu-steps", type=int, default=48)
+    ap.add_argument("--overlap-steps", type=int, default=12)
     return ap.parse_args()
 
 
@@ -75,27 +76,84 @@ def config_json(cfg: W.WorkloadConfig, n_gpus: int, miss_mode: str):
 
 
 # ---------------------------------------------------------------- clocks
-class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index: int):
-        self.index = index
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event reasons while the timed region
+    runs: NVML through ctypes every millisecond (the timed region can be a few
+    milliseconds long), else nvidia-smi every 50 ms.  Reads settings only."""
+
+    def __init__(self, cuda_index: int):
+        self.index = cuda_index
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            try:
+                self.index = int(vis.split(",")[cuda_index])
+            except (ValueError, IndexError):
+                pass
+        self.samples, self.smax, self.reasons, self.power = [], None, set(), []
         self.proc = None
+        self.thread = None
+
+    def _nvml(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvml init")
+        h = ctypes.c_void_p()
+        if nv.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(h)) != 0:
+            raise RuntimeError("nvml handle")
+        return nv, h
 
     def __enter__(self):
+        import threading
+        import ctypes
+        self.stop = False
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            nv, h = self._nvml()
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.smax = float(mx.value)
+            get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+
+            def run():
+                clk, rs, pw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+                while not self.stop:
+                    if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                        self.samples.append(float(clk.value))
+                    if get_reasons(h, ctypes.byref(rs)) == 0:
+                        for bit, name in _REASONS.items():
+                            if rs.value & bit:
+                                self.reasons.add(name)
+                    if nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0:
+                        self.power.append(pw.value / 1000.0)
+                    time.sleep(0.001)
+
+            self.thread = threading.Thread(target=run, daemon=True)
+            self.thread.start()
+            time.sleep(0.005)
         except Exception:
-            self.proc = None
+            self.thread = None
+            fields = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                      "clocks_event_reasons.hw_thermal_slowdown,"
+                      "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index), f"--query-gpu={fields}",
+                     "--format=csv,noheader,nounits", "-lms", "50"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                time.sleep(0.3)
+            except Exception:
+                self.proc = None
         return self
 
     def __exit__(self, *a):
-        self.lines = []
+        self.stop = True
+        if self.thread is not None:
+            self.thread.join(timeout=2)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -103,25 +161,26 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.splitlines():
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 6:
+                    continue
+                try:
+                    self.samples.append(float(p[0]))
+                    self.smax = float(p[1])
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[2:6]):
+                    if v.lower() == "active":
+                        self.reasons.add(n)
 
     def summary(self):
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
-            p = [x.strip() for x in l.split(",")]
-            if len(p) < 8:
-                continue
-            try:
-                sm.append(float(p[0]))
-                smax = float(p[1])
-            except ValueError:
-                continue
-            for n, v in zip(names, p[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.smax, "reasons": sorted(self.reasons),
+                "samples": len(self.samples),
+                "power_w_max": max(self.power) if self.power else None,
+                "source": "nvml" if self.thread is not None else "nvidia-smi"}
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
@@ -175,6 +234,57 @@ def bench_reference(args, cfg, rank, world):
 
 
 # ---------------------------------------------------------------- our arm
+def measure_overlap(cfg, ld, n_steps, stream, host_buffers):
+    """T_copy (staging kernel), T_SFA (attention with every row in the pool)
+    and T_fused (attention that reads misses from host memory itself), per
+    step, and OverlapRatio = (T_copy + T_SFA - T_fused) / T_copy.  A fused pool
+    runs the steps first, then a staged pool replays the same inputs from the
+    same empty state (identical selections and misses), one pool at a time."""
+    import torch
+    from host_latent_cache_gb300 import ess
+    from host_latent_cache_gb300.session import Session
+    qs = W.QueryStream(cfg)
+    wts = W.head_weights(cfg, ld.w)
+    steps = [qs.next() for _ in range(n_steps)]
+    res = {}
+    outs = {}
+    for mode in (ess.ESS_MISS_FUSED, ess.ESS_MISS_STAGED):
+        sess = Session(cfg, [ld], miss_mode=mode, host_buffers=host_buffers)
+        rows = []
+        for q, enc, qm in steps:
+            qd, wd, qmd = sess.device_inputs(enc, wts, qm)
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            sess.indexer_topk(0, qd, wd, stream)
+            e[0].record(stream)
+            if mode == ess.ESS_MISS_STAGED:
+                sess.stage(0, stream)
+            e[1].record(stream)
+            sess.attention(0, qmd, stream=stream)
+            e[2].record(stream)
+            torch.cuda.synchronize()
+            rows.append((int(sess.n_miss.sum().item()), e[0].elapsed_time(e[1]),
+                         e[1].elapsed_time(e[2])))
+        assert sess.poll(stream) == ess.ESS_OK
+        outs[mode] = sess.out.clone()
+        res[mode] = rows
+        sess.close()
+    fz, sg = res[ess.ESS_MISS_FUSED], res[ess.ESS_MISS_STAGED]
+    assert [r[0] for r in fz] == [r[0] for r in sg]
+    rng = range(1, len(fz)) if len(fz) > 1 else range(len(fz))
+    tc = statistics.mean(sg[i][1] for i in rng)
+    ts = statistics.mean(sg[i][2] for i in rng)
+    tf = statistics.mean(fz[i][2] for i in rng)
+    return {"steps": len(rng), "after_first_fill": len(fz) > 1,
+            "miss_rows_per_step": statistics.mean(fz[i][0] for i in rng),
+            "t_copy_us": 1e3 * tc, "t_sfa_us": 1e3 * ts, "t_fused_us": 1e3 * tf,
+            "overlap_ratio": (tc + ts - tf) / tc if tc > 0 else None,
+            "speedup_vs_copy_then_attend": (tc + ts) / tf if tf > 0 else None,
+            "first_fill": {"miss_rows": fz[0][0], "t_copy_us": 1e3 * sg[0][1],
+                           "t_sfa_us": 1e3 * sg[0][2], "t_fused_us": 1e3 * fz[0][2]},
+            "outputs_identical": bool(torch.equal(outs[ess.ESS_MISS_FUSED],
+                                                  outs[ess.ESS_MISS_STAGED]))}
+
+
 def bench_ours(args, cfg, rank, world, local_rank):
     import torch
     from host_latent_cache_gb300 import build as B
@@ -212,24 +322,22 @@ def bench_ours(args, cfg, rank, world, local_rank):
     out_host = torch.empty(tuple(sess.out.shape), dtype=torch.float32).pin_memory()
     stream = torch.cuda.current_stream()
     nsteps = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nsteps)]
     staged = mode == ess.ESS_MISS_STAGED
+
+    def make_events(n, k):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(k)] for _ in range(n)]
+        for row in evs:
+            for e in row:
+                e.record(stream)        # materialise the event handles
+        torch.cuda.synchronize()
+        return evs
+
+    ev = make_events(nsteps, 4)
 
     def one_step(i, events=None):
         qd, wd, qmd = dev_inputs[i]
-        if events:
-            events[0].record(stream)
-        sess.scores_only(0, qd, wd, stream)
-        if events:
-            events[1].record(stream)
-        sess.select(0, sess.scores, stream)
-        if staged:
-            sess.stage(0, stream)
-        if events:
-            events[2].record(stream)
-        sess.attention(0, qmd, stream=stream)
-        if events:
-            events[3].record(stream)
+        ess.ess_step_profiled(sess.pool, 0, qd, wd, qmd, sess.out,
+                              events if events else [None] * 4, stream)
 
     for i in range(args.warmup):
         one_step(i)
@@ -256,6 +364,12 @@ def bench_ours(args, cfg, rank, world, local_rank):
     sel_ms = [e[1].elapsed_time(e[2]) for e in ev]
     att_ms = [e[2].elapsed_time(e[3]) for e in ev]
     stats = sess.stats(0, reset=True)
+
+    # OverlapRatio of the fused miss path: fused and staged pools stepped in
+    # lockstep on the same inputs (identical state trajectories)
+    overlap = None
+    if args.overlap_steps > 0 and world == 1:
+        overlap = measure_overlap(cfg_r, ld, args.overlap_steps, stream, sess.host)
 
     # end to end through the public C ABI with host buffers
     torch.cuda.synchronize()
@@ -321,11 +435,13 @@ def bench_ours(args, cfg, rank, world, local_rank):
             "kernels_ms": {"indexer": statistics.mean(idx_ms), "select": statistics.mean(sel_ms),
                            "attention": statistics.mean(att_ms)},
             "hit_rate": stats.hits / max(stats.hits + stats.misses, 1),
+            "overlap": overlap,
             "e2e": {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": int(sum(x.numel() * x.element_size()
                                                   for x in host_inputs[0])),
                     "d2h_bytes_per_step": int(out_host.numel() * 4)},
             "gpu_launches": nsteps * (5 if staged else 4),
+            "gpu_launches_note": "per step: indexer, select, attention, combine (+ staging)",
             "clocks": clk.summary(),
         }
     sess.close()

@@ -1,9 +1,14 @@
 // Host side of the C ABI declared in ess.h: workspace layout, argument
 // checks, tensor-map encoding and the launch sequences of each entry point.
+#include <sys/mman.h>
+#include <unistd.h>
+
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "ess_internal.h"
@@ -27,6 +32,7 @@ ess_status check_config(const ess_config* c) {
   if (c->mtp > kMaxWays) return ESS_ERR_UNSUPPORTED;
   if (c->mtp * c->idx_heads > 256) return ESS_ERR_UNSUPPORTED;
   if (c->mtp > 1 && c->idx_heads % 32 != 0) return ESS_ERR_UNSUPPORTED;
+  if ((c->mtp * c->idx_heads) % 4 != 0) return ESS_ERR_UNSUPPORTED;  // 16-byte weight rows
   if (c->mla_heads > 128) return ESS_ERR_UNSUPPORTED;
   if (c->latent_dim != kLatent || c->rope_dim != kRowDim - kLatent) return ESS_ERR_UNSUPPORTED;
   if (static_cast<long long>(c->mtp) * c->k > kMaxWayK) return ESS_ERR_UNSUPPORTED;
@@ -50,6 +56,7 @@ Layout compute_layout(const ess_config& c) {
   L.o_cslots = o;   o = align256(o + B * T * 4);
   L.o_stoken = o;   o = align256(o + B * C * 4);
   L.o_lused = o;    o = align256(o + B * C * 4);
+  L.o_order = o;    o = align256(o + 2 * B * C * 4);
   L.o_pool = o;     o = align256(o + B * C * kRowBytes);
   L.layer_bytes = o;
   o = L.layer_bytes * c.n_layers;
@@ -60,7 +67,8 @@ Layout compute_layout(const ess_config& c) {
   L.o_mtok = o;     o = align256(o + B * M * k * 4);
   L.o_mslot = o;    o = align256(o + B * M * k * 4);
   L.o_nmiss = o;    o = align256(o + B * 4);
-  L.o_vict = o;     o = align256(o + B * M * k * 8);
+  L.o_vict = o;     o = align256(o + B * M * k * 4);
+  L.o_hist = o;     o = align256(o + B * M * kHistBins * 4);
   L.o_po = o;       o = align256(o + B * M * L.nch * H * kLatent * 4);
   L.o_pml = o;      o = align256(o + B * M * L.nch * H * 8);
   L.o_hq = o;       o = align256(o + B * M * HI * kKeyRowBytes);
@@ -124,6 +132,8 @@ cudaError_t launch_reset(const ess_pool& p, int layer, cudaStream_t st) {
   if ((e = cudaMemsetAsync(L.slot_token, 0xff, B * c.C * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(L.last_used, 0xff, B * c.C * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(L.step, 0, B * 4, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(p.scr.ghist, 0, B * c.mtp * kHistBins * 4, st)) != cudaSuccess) return e;
+  if ((e = launch_order_reset(p, layer, st)) != cudaSuccess) return e;
   return cudaMemsetAsync(L.stats, 0, 8 * 8, st);
 }
 
@@ -145,6 +155,64 @@ const char* ess_status_string(ess_status s) {
     case ESS_ERR_DEVICE_CHECK: return "device bounds check failed";
   }
   return "unknown status";
+}
+
+namespace {
+struct HostMapping {
+  void* base;
+  size_t len;
+};
+std::mutex g_host_mu;
+std::unordered_map<void*, HostMapping> g_host_maps;
+
+size_t thp_size() {
+  size_t sz = 2u << 20;
+  if (FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+    unsigned long long v = 0;
+    if (std::fscanf(f, "%llu", &v) == 1 && v >= 4096 && v <= (1ull << 30)) sz = v;
+    std::fclose(f);
+  }
+  return sz;
+}
+}  // namespace
+
+ess_status ess_host_alloc(size_t bytes, void** out) {
+  if (!out || bytes == 0) return ESS_ERR_INVALID_ARG;
+  *out = nullptr;
+  const size_t align = thp_size();
+  const size_t len = bytes + align;
+  void* raw = mmap(nullptr, len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+  if (raw == MAP_FAILED) return ESS_ERR_OOM;
+  char* p = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(raw) + align - 1) &
+                                    ~static_cast<uintptr_t>(align - 1));
+  madvise(p, bytes, MADV_HUGEPAGE);  // advisory; plain pages if huge pages are unavailable
+  std::memset(p, 0, bytes);
+  if (cudaHostRegister(p, bytes, cudaHostRegisterDefault) != cudaSuccess) {
+    cudaGetLastError();
+    munmap(raw, len);
+    return ESS_ERR_CUDA;
+  }
+  {
+    std::lock_guard<std::mutex> g(g_host_mu);
+    g_host_maps[p] = HostMapping{raw, len};
+  }
+  *out = p;
+  return ESS_OK;
+}
+
+ess_status ess_host_free(void* ptr) {
+  if (!ptr) return ESS_ERR_INVALID_ARG;
+  HostMapping m;
+  {
+    std::lock_guard<std::mutex> g(g_host_mu);
+    auto it = g_host_maps.find(ptr);
+    if (it == g_host_maps.end()) return ESS_ERR_INVALID_ARG;
+    m = it->second;
+    g_host_maps.erase(it);
+  }
+  const cudaError_t e = cudaHostUnregister(ptr);
+  munmap(m.base, m.len);
+  return e == cudaSuccess ? ESS_OK : ESS_ERR_CUDA;
 }
 
 ess_status ess_pool_device_bytes(const ess_config* cfg, size_t* bytes) {
@@ -195,6 +263,7 @@ ess_status ess_pool_create(const ess_config* cfg, void* dev_workspace, size_t ws
     y.cache_slots = reinterpret_cast<int32_t*>(base + L.o_cslots);
     y.slot_token = reinterpret_cast<int32_t*>(base + L.o_stoken);
     y.last_used = reinterpret_cast<int32_t*>(base + L.o_lused);
+    y.order = reinterpret_cast<int32_t*>(base + L.o_order);
     y.pool = reinterpret_cast<uint16_t*>(base + L.o_pool);
   }
   Scratch& r = p->scr;
@@ -205,7 +274,8 @@ ess_status ess_pool_create(const ess_config* cfg, void* dev_workspace, size_t ws
   r.miss_tok = reinterpret_cast<int32_t*>(p->ws + L.o_mtok);
   r.miss_slot = reinterpret_cast<int32_t*>(p->ws + L.o_mslot);
   r.n_miss = reinterpret_cast<int32_t*>(p->ws + L.o_nmiss);
-  r.vict = reinterpret_cast<unsigned long long*>(p->ws + L.o_vict);
+  r.vlist = reinterpret_cast<int32_t*>(p->ws + L.o_vict);
+  r.ghist = reinterpret_cast<uint32_t*>(p->ws + L.o_hist);
   r.part_o = reinterpret_cast<float*>(p->ws + L.o_po);
   r.part_ml = reinterpret_cast<float2*>(p->ws + L.o_pml);
   r.h_qidx = reinterpret_cast<uint8_t*>(p->ws + L.o_hq);
@@ -280,9 +350,9 @@ ess_status ess_pool_reset(ess_pool* pool, int layer, ess_stream_t stream) {
 
 ess_status ess_indexer_scores(ess_pool* pool, int layer, const void* q_idx, const float* w,
                               float* scores, ess_stream_t stream) {
-  if (!layer_ok(pool, layer) || !q_idx || !w || !scores || !aligned16(q_idx))
+  if (!layer_ok(pool, layer) || !q_idx || !w || !scores || !aligned16(q_idx) || !aligned16(w))
     return ESS_ERR_INVALID_ARG;
-  return cuda_status(launch_indexer(*pool, layer, q_idx, w, scores,
+  return cuda_status(launch_indexer(*pool, layer, q_idx, w, scores, false,
                                     static_cast<cudaStream_t>(stream)));
 }
 
@@ -292,19 +362,24 @@ ess_status ess_select_manage(ess_pool* pool, int layer, const float* scores, int
   if (!layer_ok(pool, layer) || !scores || !topk_idx || !topk_slot || !n_miss_way || !miss_tok ||
       !miss_slot || !n_miss || !aligned16(scores))
     return ESS_ERR_INVALID_ARG;
-  return cuda_status(launch_select(*pool, layer, scores, topk_idx, topk_slot, n_miss_way, miss_tok,
-                                   miss_slot, n_miss, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_select(*pool, layer, scores, false, topk_idx, topk_slot, n_miss_way,
+                                   miss_tok, miss_slot, n_miss, static_cast<cudaStream_t>(stream)));
 }
 
 ess_status ess_indexer_topk(ess_pool* pool, int layer, const void* q_idx, const float* w,
                             int32_t* topk_idx, int32_t* topk_slot, int32_t* n_miss_way,
                             int32_t* miss_tok, int32_t* miss_slot, int32_t* n_miss,
                             ess_stream_t stream) {
-  if (!layer_ok(pool, layer)) return ESS_ERR_INVALID_ARG;
-  ess_status s = ess_indexer_scores(pool, layer, q_idx, w, pool->scr.scores, stream);
-  if (s != ESS_OK) return s;
-  return ess_select_manage(pool, layer, pool->scr.scores, topk_idx, topk_slot, n_miss_way,
-                           miss_tok, miss_slot, n_miss, stream);
+  if (!layer_ok(pool, layer) || !q_idx || !w || !aligned16(q_idx) || !aligned16(w) || !topk_idx ||
+      !topk_slot ||
+      !n_miss_way || !miss_tok || !miss_slot || !n_miss)
+    return ESS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the indexer also fills the score histogram that the selection starts from
+  cudaError_t e = launch_indexer(*pool, layer, q_idx, w, pool->scr.scores, true, st);
+  if (e != cudaSuccess) return ESS_ERR_CUDA;
+  return cuda_status(launch_select(*pool, layer, pool->scr.scores, true, topk_idx, topk_slot,
+                                   n_miss_way, miss_tok, miss_slot, n_miss, st));
 }
 
 ess_status ess_stage_misses(ess_pool* pool, int layer, const int32_t* miss_tok,
@@ -326,18 +401,38 @@ ess_status ess_sparse_mla_decode(ess_pool* pool, int layer, const void* q_mla,
                                       static_cast<cudaStream_t>(stream)));
 }
 
+ess_status ess_step_profiled(ess_pool* pool, int layer, const void* q_idx, const float* w,
+                             const void* q_mla, float* out, ess_stream_t stream,
+                             void* const* events) {
+  if (!layer_ok(pool, layer) || !q_idx || !w || !q_mla || !out || !aligned16(q_idx) ||
+      !aligned16(w) || !aligned16(q_mla) || !aligned16(out))
+    return ESS_ERR_INVALID_ARG;
+  Scratch& r = pool->scr;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto mark = [&](int i) -> bool {
+    return !events || !events[i] ||
+           cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
+  };
+  if (!mark(0)) return ESS_ERR_CUDA;
+  if (launch_indexer(*pool, layer, q_idx, w, r.scores, true, st) != cudaSuccess || !mark(1))
+    return ESS_ERR_CUDA;
+  if (launch_select(*pool, layer, r.scores, true, r.topk_idx, r.topk_slot, r.n_miss_way,
+                    r.miss_tok, r.miss_slot, r.n_miss, st) != cudaSuccess)
+    return ESS_ERR_CUDA;
+  const bool staged = pool->cfg.miss_mode == ESS_MISS_STAGED;
+  if (staged && launch_stage(*pool, layer, r.miss_tok, r.miss_slot, r.n_miss, st) != cudaSuccess)
+    return ESS_ERR_CUDA;
+  if (!mark(2)) return ESS_ERR_CUDA;
+  if (launch_attention(*pool, layer, q_mla, r.topk_idx, r.topk_slot, out, staged, st) !=
+          cudaSuccess ||
+      !mark(3))
+    return ESS_ERR_CUDA;
+  return ESS_OK;
+}
+
 ess_status ess_step(ess_pool* pool, int layer, const void* q_idx, const float* w,
                     const void* q_mla, float* out, ess_stream_t stream) {
-  if (!layer_ok(pool, layer)) return ESS_ERR_INVALID_ARG;
-  Scratch& r = pool->scr;
-  ess_status s = ess_indexer_topk(pool, layer, q_idx, w, r.topk_idx, r.topk_slot, r.n_miss_way,
-                                  r.miss_tok, r.miss_slot, r.n_miss, stream);
-  if (s != ESS_OK) return s;
-  if (pool->cfg.miss_mode == ESS_MISS_STAGED) {
-    s = ess_stage_misses(pool, layer, r.miss_tok, r.miss_slot, r.n_miss, stream);
-    if (s != ESS_OK) return s;
-  }
-  return ess_sparse_mla_decode(pool, layer, q_mla, r.topk_idx, r.topk_slot, out, stream);
+  return ess_step_profiled(pool, layer, q_idx, w, q_mla, out, stream, nullptr);
 }
 
 ess_status ess_step_host(ess_pool* pool, int layer, const void* q_idx_host, const float* w_host,
@@ -348,20 +443,17 @@ ess_status ess_step_host(ess_pool* pool, int layer, const void* q_idx_host, cons
   Scratch& r = pool->scr;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t BM = static_cast<size_t>(c.batch) * c.mtp;
-  cudaError_t e;
-  if ((e = cudaMemcpyAsync(r.h_qidx, q_idx_host, BM * c.idx_heads * kKeyRowBytes,
-                           cudaMemcpyHostToDevice, st)) != cudaSuccess)
+  if (cudaMemcpyAsync(r.h_qidx, q_idx_host, BM * c.idx_heads * kKeyRowBytes,
+                      cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(r.h_w, w_host, BM * c.idx_heads * 4, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(r.h_qmla, q_mla_host, BM * c.mla_heads * kRowBytes, cudaMemcpyHostToDevice,
+                      st) != cudaSuccess)
     return ESS_ERR_CUDA;
-  if ((e = cudaMemcpyAsync(r.h_w, w_host, BM * c.idx_heads * 4, cudaMemcpyHostToDevice, st)) !=
-      cudaSuccess)
-    return ESS_ERR_CUDA;
-  if ((e = cudaMemcpyAsync(r.h_qmla, q_mla_host, BM * c.mla_heads * kRowBytes,
-                           cudaMemcpyHostToDevice, st)) != cudaSuccess)
-    return ESS_ERR_CUDA;
-  ess_status s = ess_step(pool, layer, r.h_qidx, r.h_w, r.h_qmla, r.h_out, stream);
+  const ess_status s = ess_step(pool, layer, r.h_qidx, r.h_w, r.h_qmla, r.h_out, stream);
   if (s != ESS_OK) return s;
-  if ((e = cudaMemcpyAsync(out_host, r.h_out, BM * c.mla_heads * kLatent * 4,
-                           cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+  if (cudaMemcpyAsync(out_host, r.h_out, BM * c.mla_heads * kLatent * 4, cudaMemcpyDeviceToHost,
+                      st) != cudaSuccess)
     return ESS_ERR_CUDA;
   return ESS_OK;
 }
@@ -416,10 +508,31 @@ ess_status ess_pool_set_state(ess_pool* pool, int layer, const int32_t* cache_sl
       if (slot_token[i] < -1 || slot_token[i] >= c.max_T) return ESS_ERR_INVALID_ARG;
   }
   if (cudaDeviceSynchronize() != cudaSuccess) return ESS_ERR_CUDA;
+  // the LRU order list is derived from last_used and step: rebuild it
+  std::vector<int32_t> lu(B * c.C), sp(B);
+  if (last_used) std::memcpy(lu.data(), last_used, lu.size() * 4);
+  else if (cudaMemcpy(lu.data(), L.last_used, lu.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess) return ESS_ERR_CUDA;
+  if (step) std::memcpy(sp.data(), step, sp.size() * 4);
+  else if (cudaMemcpy(sp.data(), L.step, sp.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess) return ESS_ERR_CUDA;
+  for (size_t b = 0; b < B; ++b) {
+    if (sp[b] < 0) return ESS_ERR_INVALID_ARG;
+    for (int i = 0; i < c.C; ++i)
+      if (lu[b * c.C + i] < -1 || lu[b * c.C + i] >= sp[b]) return ESS_ERR_INVALID_ARG;
+  }
   if (cache_slots && cudaMemcpy(L.cache_slots, cache_slots, B * c.max_T * 4, cudaMemcpyHostToDevice) != cudaSuccess) return ESS_ERR_CUDA;
   if (slot_token && cudaMemcpy(L.slot_token, slot_token, B * c.C * 4, cudaMemcpyHostToDevice) != cudaSuccess) return ESS_ERR_CUDA;
   if (last_used && cudaMemcpy(L.last_used, last_used, B * c.C * 4, cudaMemcpyHostToDevice) != cudaSuccess) return ESS_ERR_CUDA;
   if (step && cudaMemcpy(L.step, step, B * 4, cudaMemcpyHostToDevice) != cudaSuccess) return ESS_ERR_CUDA;
+  std::vector<int32_t> ord(c.C);
+  for (size_t b = 0; b < B; ++b) {
+    for (int i = 0; i < c.C; ++i) ord[i] = i;
+    const int32_t* l = lu.data() + b * c.C;
+    std::sort(ord.begin(), ord.end(), [l](int32_t x, int32_t y) {
+      return l[x] != l[y] ? l[x] < l[y] : x < y;
+    });
+    int32_t* dst = L.order + (static_cast<size_t>(sp[b] & 1) * B + b) * c.C;
+    if (cudaMemcpy(dst, ord.data(), c.C * 4, cudaMemcpyHostToDevice) != cudaSuccess) return ESS_ERR_CUDA;
+  }
   return ESS_OK;
 }
 

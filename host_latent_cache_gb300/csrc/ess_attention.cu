@@ -15,10 +15,16 @@
 // CTAs.  Rows are gathered with 16-byte cp.async straight from the pool
 // (HBM) or from pinned host memory (UVA) into 128B-swizzled shared memory;
 // tcgen05.mma computes S[128 heads][128 rows] = Q * R^T (bf16, fp32 in
-// TMEM) one 64-dim block at a time as rows land, the softmax numerator P is
-// formed in fp32 and stored as fp16, the 512 value dims of the rows are
-// converted in place to fp16, and O[128][512] = P * V accumulates in TMEM.
-// Per-CTA (max, sum, O) partials are merged by a second kernel.
+// TMEM) one 64-dim block at a time as rows land; the softmax numerator P is
+// formed in fp32 and split into two bf16 terms P = P_hi + P_lo (about 16
+// significant bits, so the output stays within the tolerance), and
+// O[128][512] = P_hi * V + P_lo * V accumulates in TMEM with V read in place
+// as the N-major operand.
+// Per-CTA (max, sum, O) partials are merged across the chunks of a (request,
+// way): when the chunk CTAs form one thread-block cluster, CTA r reads the
+// others' (max, sum) through distributed shared memory and reduces output
+// dims [r*512/nch, (r+1)*512/nch) from the partials in L2; otherwise a second
+// kernel merges them.
 #include "ess_device.cuh"
 
 namespace ess {
@@ -44,6 +50,8 @@ struct AttnArgs {
   int B, M, H, k, nch, C, T, page, npages;
   float c2;                   // sm_scale * log2(e)
   int staged;
+  int fused_combine;          // 1: the nch chunk CTAs are one cluster and merge in place
+  float* out;                 // [B][M][H][512] (fused combine)
 };
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -61,6 +69,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* ofull = sfull + 1;                // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ofull + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  __shared__ float2 ml_s[kAttnRows];          // this CTA's (max, sum) per head
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -103,8 +112,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   }
 
-  // ------------------------------------------------ gather: thread j owns row j
+  // ------------------------------------------------ gather
+  // Thread j resolves row j (its entry, hit/miss, source address); warp w then
+  // gathers its rows 32w..32w+31 cooperatively: for each 64-dim block, 8 lanes
+  // cover one row's 128 bytes, so every instruction moves four full lines.
   const int j = tid;
+  const int lane = tid & 31;
   bool valid = j < cnt;
   bool miss = false;
   int slot = 0;
@@ -129,12 +142,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       src = a.pool + (static_cast<size_t>(b) * a.C + slot) * kRowDim;
     }
   }
+  const unsigned valid_mask = __ballot_sync(0xffffffffu, valid);
+  const int sub = lane >> 3;   // row within a group of four
+  const int ch = lane & 7;     // 16-byte chunk within the 128-byte block row
   for (int kb = 0; kb < kDimBlocks; ++kb) {
     uint8_t* dst = rows + kb * kBlk;
-    for (int ch = 0; ch < 8; ++ch) {
-      const uint32_t off = sw128_off(j, ch);
-      if (valid)
-        cp_async16(smem_u32(dst + off), src + kb * 64 + ch * 8);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int rl = q * 4 + sub;                 // row of this warp, 0..31
+      const int r = warp * 32 + rl;
+      const uint64_t sp = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(src), rl);
+      const uint32_t off = sw128_off(r, ch);
+      if ((valid_mask >> rl) & 1u)
+        cp_async16(smem_u32(dst + off), reinterpret_cast<const uint16_t*>(sp) + kb * 64 + ch * 8);
       else
         *reinterpret_cast<uint4*>(dst + off) = make_uint4(0, 0, 0, 0);
     }
@@ -179,14 +199,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   if (tid == 0 && ok) umma_commit(smem_u32(sfull));
 
-  // FUSED miss path: write the host row through to its pool slot
-  if (valid && miss && !a.staged) {
-    uint16_t* dstp = a.pool + (static_cast<size_t>(b) * a.C + slot) * kRowDim;
-    for (int kb = 0; kb < kDimBlocks; ++kb)
-      for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(dstp + kb * 64 + ch * 8) =
-            *reinterpret_cast<const uint4*>(rows + kb * kBlk + sw128_off(j, ch));
+  // FUSED miss path: write each host row through to its pool slot (the warp
+  // that gathered the row copies it, 16 bytes per lane)
+  cp_async_wait<0>();
+  __syncwarp();
+  {
+    const unsigned miss_mask = __ballot_sync(0xffffffffu, valid && miss && !a.staged);
+    for (unsigned mm = miss_mask; mm; mm &= mm - 1) {
+      const int rl = __ffs(mm) - 1;
+      const int r = warp * 32 + rl;
+      const int sl = __shfl_sync(0xffffffffu, slot, rl);
+      uint16_t* dstp = a.pool + (static_cast<size_t>(b) * a.C + sl) * kRowDim;
+      for (int q = lane; q < kRowBytes / 16; q += 32) {
+        const int kb = q >> 3, cc = q & 7;
+        *reinterpret_cast<uint4*>(dstp + kb * 64 + cc * 8) =
+            *reinterpret_cast<const uint4*>(rows + kb * kBlk + sw128_off(r, cc));
+      }
+    }
   }
+  __syncwarp();
 
   // ------------------------------------------------ softmax over this CTA's rows
   const bool s_ok = mbar_wait(smem_u32(sfull), 0, abort_flag);
@@ -203,7 +234,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (cc * 32 + i < cnt) mx = fmaxf(mx, v[i]);
     }
     const float base = (cnt > 0) ? mx * a.c2 : 0.0f;
-    uint8_t* P = qst;  // [128 heads x 128 rows] fp16, two 64-row blocks
+    // [128 heads x 128 rows] bf16, two 64-row blocks each: P_hi in stages 0-1,
+    // P_lo in stages 2-3 (the query stages are free once S is complete)
+    uint8_t* Phi = qst;
+    uint8_t* Plo = qst + 2 * kBlk;
     for (int cc = 0; cc < 4; ++cc) {
       float v[32];
       tmem_ld32(trow + cc * 32, v);
@@ -216,54 +250,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {  // 4 chunks of 8 rows
         const int col = cc * 32 + q * 8;
-        uint4 pk;
-        __half2 h0 = __floats2half2_rn(p[q * 8 + 0], p[q * 8 + 1]);
-        __half2 h1 = __floats2half2_rn(p[q * 8 + 2], p[q * 8 + 3]);
-        __half2 h2 = __floats2half2_rn(p[q * 8 + 4], p[q * 8 + 5]);
-        __half2 h3 = __floats2half2_rn(p[q * 8 + 6], p[q * 8 + 7]);
-        pk.x = *reinterpret_cast<uint32_t*>(&h0);
-        pk.y = *reinterpret_cast<uint32_t*>(&h1);
-        pk.z = *reinterpret_cast<uint32_t*>(&h2);
-        pk.w = *reinterpret_cast<uint32_t*>(&h3);
-        *reinterpret_cast<uint4*>(P + (col >> 6) * kBlk + sw128_off(tid, (col & 63) >> 3)) = pk;
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = p[q * 8 + 2 * e], x1 = p[q * 8 + 2 * e + 1];
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+          const float2 hf = __bfloat1622float2(h2);
+          const __nv_bfloat162 l2 = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+          hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
+        }
+        const uint32_t off = (col >> 6) * kBlk + sw128_off(tid, (col & 63) >> 3);
+        *reinterpret_cast<uint4*>(Phi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(Plo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
     }
     mx = (cnt > 0) ? base : -INFINITY;
-    // value dims of this thread's row: bf16 -> fp16 in place (blocks 0..7)
-    bool over = false;
-    for (int kb = 0; kb < kLatent / 64; ++kb) {
-      for (int ch = 0; ch < 8; ++ch) {
-        uint4* pp = reinterpret_cast<uint4*>(rows + kb * kBlk + sw128_off(j, ch));
-        uint4 u = *pp;
-        uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float lo = __uint_as_float(w4[q] << 16);
-          const float hi = __uint_as_float(w4[q] & 0xffff0000u);
-          over |= fabsf(lo) > 65504.0f || fabsf(hi) > 65504.0f;
-          __half2 h = __floats2half2_rn(lo, hi);
-          w4[q] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        *pp = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
-    }
-    if (over) set_status(a.status, ESS_ERR_UNSUPPORTED);
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && all_ok) {
     tc_fence_after();
-    // O[128 x 512] = P[128 x 128] * V[128 x 512]; V is N-major (dims contiguous)
-    const uint32_t idesc_pv = make_idesc(kFmtF16, kFmtF16, 1, 256, 128);
-    const uint32_t pa = smem_u32(qst);
+    // O[128 x 512] = (P_hi + P_lo)[128 x 128] * V[128 x 512]; V is N-major (dims contiguous)
+    const uint32_t idesc_pv = make_idesc(kFmtBF16, kFmtBF16, 1, 256, 128);
     const uint32_t ra = smem_u32(rows);
     for (int kt = 0; kt < 8; ++kt) {
-      const uint64_t ad = make_sdesc_sw128(pa + (kt >> 2) * kBlk + (kt & 3) * 32, 16, 1024);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const uint64_t bd = make_sdesc_sw128(ra + half * 4 * kBlk + kt * 2048, kBlk, 1024);
-        umma_f16(tmem + half * 256, ad, bd, idesc_pv, kt > 0);
+      for (int part = 0; part < 2; ++part) {
+        const uint32_t pa = smem_u32(qst + part * 2 * kBlk);
+        const uint64_t ad = make_sdesc_sw128(pa + (kt >> 2) * kBlk + (kt & 3) * 32, 16, 1024);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint64_t bd = make_sdesc_sw128(ra + half * 4 * kBlk + kt * 2048, kBlk, 1024);
+          umma_f16(tmem + half * 256, ad, bd, idesc_pv, (kt | part) != 0);
+        }
       }
     }
     umma_commit(smem_u32(ofull));
@@ -273,22 +294,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const bool all_o = __syncthreads_and(o_ok ? 1 : 0) != 0;
   const size_t pr = (static_cast<size_t>(b) * a.M + m) * a.nch + c;
   if (all_o) {
+    // partial O stored heads-fastest ([dim][head]) so a warp's stores coalesce
     tc_fence_after();
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float* dst = a.part_o + (pr * a.H + tid) * kLatent;
+    float* dst = a.part_o + pr * kLatent * a.H + tid;
     for (int cc = 0; cc < kLatent / 32; ++cc) {
       float v[32];
       tmem_ld32(trow + cc * 32, v);
       if (tid < a.H) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float4*>(dst + cc * 32 + q * 4) =
-              make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+        for (int i = 0; i < 32; ++i) dst[static_cast<size_t>(cc * 32 + i) * a.H] = v[i];
       }
     }
     if (tid < a.H) a.part_ml[pr * a.H + tid] = make_float2(mx, l);
-  } else if (tid < a.H) {
-    a.part_ml[pr * a.H + tid] = make_float2(-INFINITY, 0.0f);
+    ml_s[tid] = make_float2(mx, l);
+  } else {
+    if (tid < a.H) a.part_ml[pr * a.H + tid] = make_float2(-INFINITY, 0.0f);
+    ml_s[tid] = make_float2(-INFINITY, 0.0f);
   }
   tc_fence_before();
   __syncthreads();
@@ -296,36 +318,94 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (a.fused_combine) {
+    // merge the chunk partials of this (request, way) inside the cluster
+    const int nch = a.nch;
+    const int dpc = kLatent / nch;     // output dims reduced by this CTA
+    const int d0 = c * dpc;
+    cluster_sync();                    // partials (global) and ml_s of every chunk visible
+    float wgt[16];
+    float M = -INFINITY, L = 0.0f;
+    const uint32_t mla = smem_u32(&ml_s[tid]);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) wgt[q] = 0.0f;
+    float2 mlv[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      mlv[q] = q < nch ? ld_dsmem_f2(dsmem_addr(mla, static_cast<uint32_t>(q)))
+                       : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) M = fmaxf(M, mlv[q].x);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const float wv = (M != -INFINITY && mlv[q].y > 0.0f) ? exp2f(mlv[q].x - M) : 0.0f;
+      wgt[q] = wv;
+      L += wv * mlv[q].y;
+    }
+    cluster_sync();                    // every CTA has read the others' ml_s
+    if (tid < a.H) {
+      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      const size_t bm = static_cast<size_t>(b) * a.M + m;
+      const float* po = a.part_o + bm * nch * kLatent * a.H + static_cast<size_t>(d0) * a.H + tid;
+      float* o = a.out + (bm * a.H + tid) * kLatent + d0;
+      for (int db = 0; db < dpc; db += 32) {
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          if (q >= nch || wgt[q] == 0.0f) continue;
+          const float* pc = po + static_cast<size_t>(q) * kLatent * a.H + static_cast<size_t>(db) * a.H;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = fmaf(wgt[q], __ldg(pc + static_cast<size_t>(i) * a.H), acc[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(o + db + i) =
+              make_float4(acc[i] * inv, acc[i + 1] * inv, acc[i + 2] * inv, acc[i + 3] * inv);
+      }
+    }
+  }
 }
 
-// out[b][m][h][:] = sum_c 2^(mx_c - M) O_c / sum_c 2^(mx_c - M) l_c
+// out[b][m][h][d] = sum_c 2^(mx_c - M) O_c[d][h] / sum_c 2^(mx_c - M) l_c
+// One CTA per (request, way) and block of 32 dims; thread h handles head h.
+constexpr int kCombMaxCh = 64;
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
                                                       const float2* __restrict__ part_ml,
                                                       float* __restrict__ out, int H, int nch) {
-  const int row = blockIdx.x;            // (b*M + m)*H + h
-  const int bm = row / H, h = row % H;
+  const int bm = blockIdx.x;
+  const int d0 = blockIdx.y * 32;
+  const int h = threadIdx.x;
+  if (h >= H) return;
   const float2* ml = part_ml + static_cast<size_t>(bm) * nch * H + h;
+  float wgt[kCombMaxCh];
   float M = -INFINITY;
   for (int c = 0; c < nch; ++c) M = fmaxf(M, ml[static_cast<size_t>(c) * H].x);
-  float4 acc = make_float4(0, 0, 0, 0);
   float L = 0.0f;
-  if (M != -INFINITY) {
-    for (int c = 0; c < nch; ++c) {
-      const float2 v = ml[static_cast<size_t>(c) * H];
-      if (v.y <= 0.0f) continue;
-      const float wgt = exp2f(v.x - M);
-      L += wgt * v.y;
-      const float4 o = *reinterpret_cast<const float4*>(
-          part_o + ((static_cast<size_t>(bm) * nch + c) * H + h) * kLatent + threadIdx.x * 4);
-      acc.x = fmaf(wgt, o.x, acc.x);
-      acc.y = fmaf(wgt, o.y, acc.y);
-      acc.z = fmaf(wgt, o.z, acc.z);
-      acc.w = fmaf(wgt, o.w, acc.w);
-    }
+  for (int c = 0; c < nch; ++c) {
+    const float2 v = ml[static_cast<size_t>(c) * H];
+    const float wv = (M != -INFINITY && v.y > 0.0f) ? exp2f(v.x - M) : 0.0f;
+    wgt[c] = wv;
+    L += wv * v.y;
   }
   const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-  *reinterpret_cast<float4*>(out + static_cast<size_t>(row) * kLatent + threadIdx.x * 4) =
-      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  const float* po = part_o + static_cast<size_t>(bm) * nch * kLatent * H + static_cast<size_t>(d0) * H + h;
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+  for (int c = 0; c < nch; ++c) {
+    const float wv = wgt[c];
+    if (wv == 0.0f) continue;            // also skips partials of empty chunks
+    const float* pc = po + static_cast<size_t>(c) * kLatent * H;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = fmaf(wv, __ldg(pc + static_cast<size_t>(i) * H), acc[i]);
+  }
+  float* o = out + (static_cast<size_t>(bm) * H + h) * kLatent + d0;
+#pragma unroll
+  for (int i = 0; i < 32; i += 4)
+    *reinterpret_cast<float4*>(o + i) = make_float4(acc[i] * inv, acc[i + 1] * inv, acc[i + 2] * inv,
+                                                    acc[i + 3] * inv);
 }
 
 // (a6) one warp per miss row: host row of miss_tok -> pool slot miss_slot
@@ -400,11 +480,55 @@ cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(a.nch, c.mtp, c.batch);
+  a.out = out;
+  a.fused_combine = 0;
+  // the chunks of one (request, way) form a cluster when they can: nch divides
+  // 512 into whole 32-dim slices and the device schedules clusters of nch CTAs
+  static int cluster_ok[17] = {0};   // 0 unknown, 1 yes, -1 no (per cluster size)
+  const int nch = a.nch;
+  if (nch >= 1 && nch <= 16 && (kLatent % nch) == 0 && ((kLatent / nch) % 32) == 0) {
+    if (cluster_ok[nch] == 0) {
+      cluster_ok[nch] = -1;
+      if (nch > 8)
+        cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      cudaLaunchConfig_t cfgq = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = nch;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfgq.gridDim = grid;
+      cfgq.blockDim = dim3(kAttnThreads);
+      cfgq.dynamicSmemBytes = smem;
+      cfgq.attrs = at;
+      cfgq.numAttrs = 1;
+      int ncl = 0;
+      if (cudaOccupancyMaxActiveClusters(&ncl, attn_kernel, &cfgq) == cudaSuccess && ncl > 0)
+        cluster_ok[nch] = 1;
+      cudaGetLastError();
+    }
+    a.fused_combine = cluster_ok[nch] > 0 ? 1 : 0;
+  }
+  if (a.fused_combine) {
+    cudaLaunchConfig_t cfgl = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = nch;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfgl.gridDim = grid;
+    cfgl.blockDim = dim3(kAttnThreads);
+    cfgl.dynamicSmemBytes = smem;
+    cfgl.stream = st;
+    cfgl.attrs = at;
+    cfgl.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfgl, attn_kernel, qmap, a);
+  }
   attn_kernel<<<grid, kAttnThreads, smem, st>>>(qmap, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  combine_kernel<<<c.batch * c.mtp * c.mla_heads, 128, 0, st>>>(p.scr.part_o, p.scr.part_ml, out,
-                                                                c.mla_heads, a.nch);
+  combine_kernel<<<dim3(c.batch * c.mtp, kLatent / 32), 128, 0, st>>>(p.scr.part_o, p.scr.part_ml,
+                                                                      out, c.mla_heads, a.nch);
   return cudaGetLastError();
 }
 

@@ -7,14 +7,20 @@
 //     S = fl32( scale_s * sum_h w_h * ReLU(q_h . k_s) ).
 //
 // Persistent, warp-specialised kernel, one CTA per SM:
-//   warp 0     loads the queries of the current request into shared memory
-//              and streams 128-token key tiles (128 B per token) with TMA
-//              into a 6-stage ring;
+//   warp 0     (one lane) streams 128-token key tiles (128 B per token) with
+//              TMA into a 6-stage ring, and at each request boundary starts
+//              asynchronous loads of that request's queries (TMA, 128B
+//              swizzle) and head weights (bulk copy) without pausing the
+//              key stream;
 //   warp 1     (one lane) issues tcgen05.mma: D[128 tokens][N] = K_tile * Q^T
 //              with e4m3 (kind::f8f6f4) or bf16 (kind::f16) inputs and fp32
 //              accumulators in TMEM, N = ways x heads padded to 32;
-//   warps 2-5  read a token row of D from TMEM per thread, apply ReLU, the
-//              head weights and the key scale, and store the scores.
+//   warps 2-9  two groups of four epilogue warps taking alternate tiles: a
+//              thread reads its token's row of D from TMEM, applies ReLU, the
+//              head weights and the key scale, stores the score and counts it
+//              in a shared-memory histogram of the top 12 bits of its ordered
+//              key, which is added to a per-(request, way) global histogram
+//              at the end of each request's run of tiles.
 // The key tiles are the only large HBM stream; the kernel is bound by HBM
 // bandwidth (about 132 B per token and request).
 #include "ess_device.cuh"
@@ -29,6 +35,7 @@ struct IdxArgs {
   const int32_t* tile_off;   // [B+1]
   const uint8_t* q;          // [B][M][H_I][128 B]
   float* scores;             // [B][M][T]
+  uint32_t* ghist;           // [B][M][kHistBins] or null
   int* status;
   int B, M, HI, NP, T, total_tiles, A;
 };
@@ -44,7 +51,8 @@ __device__ __forceinline__ int find_request(const int32_t* tile_off, int B, int 
 
 template <bool FP8>
 __global__ void __launch_bounds__(kIdxThreads, 1)
-    indexer_kernel(const __grid_constant__ CUtensorMap kmap, const IdxArgs a) {
+    indexer_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                   const IdxArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -53,14 +61,17 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   uint8_t* kst = smem;                                   // S x 16 KB key tiles
   uint8_t* qbuf = kst + S * kTileBytes;                  // 2 x NP x 128 B queries
   float* wbuf = reinterpret_cast<float*>(qbuf + 2 * NP * 128);  // 2 x NP weights
-  uint64_t* bars = reinterpret_cast<uint64_t*>(wbuf + 2 * NP);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + 2 * NP);   // 2 x M x kHistBins
+  const int HB = a.ghist ? a.M * kHistBins : 0;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(hist + 2 * HB);
   uint64_t* full = bars;
   uint64_t* empty = full + S;
   uint64_t* accf = empty + S;
   uint64_t* acce = accf + 4;
   uint64_t* qfull = acce + 4;
   uint64_t* qempty = qfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qempty + 2);
+  uint64_t* epdone = qempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epdone + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* consumed = abort_flag + 1;
 
@@ -84,19 +95,25 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&qfull[i]), 1);
-      mbar_init(smem_u32(&qempty[i]), 1 + 128);
+      mbar_init(smem_u32(&qempty[i]), 1 + 256);
+      mbar_init(smem_u32(&epdone[i]), 256);
     }
     *abort_flag = 0;
     *consumed = 0;
     fence_mbar_init();
   }
+  for (int i = tid; i < 2 * HB; i += kIdxThreads) hist[i] = 0;
+  for (int i = tid; i < 2 * NP; i += kIdxThreads) wbuf[i] = 0.0f;
   uint32_t ncols = 32;
   while (ncols < static_cast<uint32_t>(A * NP)) ncols <<= 1;
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), ncols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&kmap);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&qmap);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -113,31 +130,25 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       if (b != cur_b) {
         ++seg;
         const int qb = seg & 1;
-        if (seg >= 2) {
-          int w_ok = 1;
-          if (lane == 0)
+        int w_ok = 1;
+        if (lane == 0) {
+          if (seg >= 2)
             w_ok = mbar_wait(smem_u32(&qempty[qb]), ((seg >> 1) - 1) & 1, abort_flag) ? 1 : 0;
-          w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-          if (!w_ok) {
-            ok = false;
-            break;
+          if (w_ok) {
+            // queries: NP rows x 128 B by TMA (128B swizzle = the MMA operand
+            // layout; rows past M*H_I belong to other requests or are zero and
+            // only meet zero weights); weights: M*H_I floats by bulk copy
+            mbar_arrive_expect_tx(smem_u32(&qfull[qb]), static_cast<uint32_t>(NP * 128 + MH * 4));
+            tma_load_2d(smem_u32(qbuf + qb * NP * 128), &qmap, smem_u32(&qfull[qb]), 0, b * MH);
+            bulk_load(smem_u32(wbuf + qb * NP), a.w + static_cast<size_t>(b) * MH,
+                      static_cast<uint32_t>(MH * 4), smem_u32(&qfull[qb]));
           }
         }
-        // queries: NP rows x 128 B, 128B-swizzled, zero rows past M*H_I
-        uint8_t* qd = qbuf + qb * NP * 128;
-        const uint8_t* qs = a.q + static_cast<size_t>(b) * MH * 128;
-        for (int c = lane; c < NP * 8; c += 32) {
-          const int row = c >> 3, ch = c & 7;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (row < MH) v = __ldg(reinterpret_cast<const uint4*>(qs + row * 128 + ch * 16));
-          *reinterpret_cast<uint4*>(qd + sw128_off(row, ch)) = v;
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) {
+          ok = false;
+          break;
         }
-        float* wd = wbuf + qb * NP;
-        for (int n = lane; n < NP; n += 32)
-          wd[n] = (n < MH) ? __ldg(a.w + static_cast<size_t>(b) * MH + n) : 0.0f;
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&qfull[qb]));
         cur_b = b;
       }
       int w_ok = 1;
@@ -202,13 +213,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       if (seg >= 0) umma_commit(smem_u32(&qempty[seg & 1]));
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------ epilogue (warps 2..9)
+    const int grp = (warp - 2) >> 2;         // tiles with it % 2 == grp
     const int quad = warp & 3;               // TMEM lanes 32*quad .. +31
     const int row = quad * 32 + lane;        // token row of the tile
+    const int te = tid - 64;                 // 0..255
     int b = find_request(a.tile_off, a.B, g0);
     int cur_b = -1, seg = -1, it = 0;
     int Tcur = 0;
-    for (int g = g0; g < g1; ++g, ++it) {
+    bool ok = true;
+    for (int g = g0; g < g1 && ok; ++g, ++it) {
       while (b + 1 < a.B && g >= a.tile_off[b + 1]) ++b;
       const int j = g - a.tile_off[b];
       if (b != cur_b) {
@@ -217,45 +231,90 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         cur_b = b;
         Tcur = a.Tb[b];
       }
-      // issue the scale load before waiting so its latency hides under the wait
-      const int t = j * kIdxTile + row;
-      const bool in_range = t < Tcur;
-      float sc = 1.0f;
-      if (a.scale != nullptr && in_range) sc = __ldg(a.scale + static_cast<size_t>(b) * a.T + t);
-      const int acc = it % A;
-      if (!mbar_wait(smem_u32(&accf[acc]), (it / A) & 1, abort_flag)) break;
-      tc_fence_after();
-      const float* wq = wbuf + (seg & 1) * NP;
-      float sm[kMaxWays];
+      if ((it & 1) == grp) {
+        // issue the scale load before waiting so its latency hides under the wait
+        const int t = j * kIdxTile + row;
+        const bool in_range = t < Tcur;
+        float sc = 1.0f;
+        if (a.scale != nullptr && in_range) sc = __ldg(a.scale + static_cast<size_t>(b) * a.T + t);
+        const int acc = it % A;
+        ok = mbar_wait(smem_u32(&accf[acc]), (it / A) & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const float* wq = wbuf + (seg & 1) * NP;
+        float sm[kMaxWays];
 #pragma unroll
-      for (int m = 0; m < kMaxWays; ++m) sm[m] = 0.0f;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                             static_cast<uint32_t>(acc * NP);
-      for (int c = 0; c < NP / 32; ++c) {
-        float v[32];
-        tmem_ld32(taddr + c * 32, v);
-        // columns n = c*32 + i belong to way n / H_I (H_I % 32 == 0 or M == 1)
-        const int m = (a.M == 1) ? 0 : (c * 32) / a.HI;
-        float part = 0.0f;
+        for (int m = 0; m < kMaxWays; ++m) sm[m] = 0.0f;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                               static_cast<uint32_t>(acc * NP);
+        // every product and partial sum is exact under the score contract, so
+        // four independent chains per chunk give the same result as one
+        if (NP == 32) {
+          float v[32];
+          tmem_ld32(taddr, v);
+          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) part = fmaf(wq[c * 32 + i], fmaxf(v[i], 0.0f), part);
-        // every term is exact under the score contract, so the order is free
-        if (m == 0) sm[0] += part;
-        else if (m == 1) sm[1] += part;
-        else if (m == 2) sm[2] += part;
-        else sm[3] += part;
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&acce[acc]));
-      if (in_range) {
-        for (int m = 0; m < a.M; ++m) {
-          const float s = __fmul_rn(sm[m], sc) + 0.0f;  // one rounding; +0 for a zero score
-          a.scores[(static_cast<size_t>(b) * a.M + m) * a.T + t] = s;
+          for (int i = 0; i < 32; i += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(wq + i);
+            p0 = fmaf(w4.x, fmaxf(v[i], 0.0f), p0);
+            p1 = fmaf(w4.y, fmaxf(v[i + 1], 0.0f), p1);
+            p2 = fmaf(w4.z, fmaxf(v[i + 2], 0.0f), p2);
+            p3 = fmaf(w4.w, fmaxf(v[i + 3], 0.0f), p3);
+          }
+          sm[0] = (p0 + p1) + (p2 + p3);
+        } else {
+          for (int c = 0; c < NP / 64; ++c) {
+            float v[64];
+            tmem_ld64(taddr + c * 64, v);
+            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 64; i += 4) {
+              const float4 w4 = *reinterpret_cast<const float4*>(wq + c * 64 + i);
+              p0 = fmaf(w4.x, fmaxf(v[i], 0.0f), p0);
+              p1 = fmaf(w4.y, fmaxf(v[i + 1], 0.0f), p1);
+              p2 = fmaf(w4.z, fmaxf(v[i + 2], 0.0f), p2);
+              p3 = fmaf(w4.w, fmaxf(v[i + 3], 0.0f), p3);
+            }
+            const float part = (p0 + p1) + (p2 + p3);
+            // columns n = c*64 + i belong to way n / H_I (H_I % 32 == 0 or M == 1)
+            const int m = (a.M == 1) ? 0 : (c * 64) / a.HI;
+            if (m == 0) sm[0] += part;
+            else if (m == 1) sm[1] += part;
+            else if (m == 2) sm[2] += part;
+            else sm[3] += part;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&acce[acc]));
+        if (in_range) {
+          uint32_t* hseg = hist + (seg & 1) * HB;
+          for (int m = 0; m < a.M; ++m) {
+            const float sv = __fmul_rn(sm[m], sc) + 0.0f;  // one rounding; +0 for a zero score
+            a.scores[(static_cast<size_t>(b) * a.M + m) * a.T + t] = sv;
+            if (HB) atomicAdd(hseg + m * kHistBins + (float_key(sv) >> 20), 1u);
+          }
         }
       }
-      // end of this request's segment: release the query buffer
+      // end of this request's run of tiles: release the query buffer and
+      // publish the histogram once every epilogue thread has counted
       const bool last = (g + 1 == g1) || (g + 1 >= a.tile_off[b + 1]);
-      if (last) mbar_arrive(smem_u32(&qempty[seg & 1]));
+      if (last) {
+        mbar_arrive(smem_u32(&qempty[seg & 1]));
+        if (HB) {
+          mbar_arrive(smem_u32(&epdone[seg & 1]));
+          if (!mbar_wait(smem_u32(&epdone[seg & 1]), (seg >> 1) & 1, abort_flag)) break;
+          uint32_t* hseg = hist + (seg & 1) * HB;
+          uint32_t* gh = a.ghist + static_cast<size_t>(b) * a.M * kHistBins;
+          for (int i = te; i < HB; i += 256) {
+            const uint32_t v = hseg[i];
+            if (v) {
+              atomicAdd(gh + i, v);
+              hseg[i] = 0;
+            }
+          }
+        }
+      }
     }
   }
 
@@ -267,15 +326,15 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   }
 }
 
-size_t indexer_smem_bytes(int NP) {
+size_t indexer_smem_bytes(int NP, int HB) {
   return 1024 + static_cast<size_t>(S) * kTileBytes + 2u * NP * 128 + 2u * NP * 4 +
-         (2 * S + 8 + 4) * 8 + 16;
+         2u * HB * 4 + (2 * S + 8 + 6) * 8 + 16;
 }
 
 }  // namespace
 
 cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, const float* w,
-                           float* scores, cudaStream_t st) {
+                           float* scores, bool with_hist, cudaStream_t st) {
   const ess_config& c = p.cfg;
   const Layer& L = p.layers[layer];
   if (L.total_tiles == 0) return cudaSuccess;
@@ -286,6 +345,7 @@ cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, cons
   a.tile_off = L.tile_off;
   a.q = static_cast<const uint8_t*>(q_idx);
   a.scores = scores;
+  a.ghist = with_hist ? p.scr.ghist : nullptr;
   a.status = p.scr.status;
   a.B = c.batch;
   a.M = c.mtp;
@@ -294,19 +354,24 @@ cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, cons
   a.T = c.max_T;
   a.total_tiles = L.total_tiles;
   a.A = 512 / a.NP < 4 ? 512 / a.NP : 4;
+  CUtensorMap qmap;
+  if (!encode_map_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_idx, kKeyRowBytes,
+                     static_cast<uint64_t>(c.batch) * c.mtp * c.idx_heads, kKeyRowBytes,
+                     kKeyRowBytes, static_cast<uint32_t>(a.NP)))
+    return cudaErrorInvalidValue;
   const int grid = L.total_tiles < p.num_sms ? L.total_tiles : p.num_sms;
-  const size_t smem = indexer_smem_bytes(a.NP);
+  const size_t smem = indexer_smem_bytes(a.NP, with_hist ? c.mtp * kHistBins : 0);
   cudaError_t e;
   if (c.idx_dtype == ESS_FP8_E4M3) {
     e = cudaFuncSetAttribute(indexer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    indexer_kernel<true><<<grid, kIdxThreads, smem, st>>>(L.kmap, a);
+    indexer_kernel<true><<<grid, kIdxThreads, smem, st>>>(L.kmap, qmap, a);
   } else {
     e = cudaFuncSetAttribute(indexer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    indexer_kernel<false><<<grid, kIdxThreads, smem, st>>>(L.kmap, a);
+    indexer_kernel<false><<<grid, kIdxThreads, smem, st>>>(L.kmap, qmap, a);
   }
   return cudaGetLastError();
 }

@@ -17,7 +17,8 @@ constexpr int kMaxWays = 4;
 constexpr int kMaxWayK = 8192;        // M * k cap of the selection lists
 constexpr int kKeyRowBytes = 128;     // one indexer key row
 
-constexpr int kIdxThreads = 192;      // 6 warps: TMA, MMA, 4 epilogue
+constexpr int kIdxThreads = 320;      // 10 warps: TMA, MMA, 2 groups of 4 epilogue warps
+constexpr int kHistBins = 4096;       // score histogram on the top 12 bits of the ordered key
 constexpr int kIdxStages = 6;         // key-tile ring
 constexpr int kIdxTile = 128;         // tokens per tile (MMA M)
 
@@ -48,6 +49,7 @@ struct Layer {
   int32_t* slot_token = nullptr;  // [B][C]
   int32_t* last_used = nullptr;   // [B][C]
   int32_t* step = nullptr;        // [B]
+  int32_t* order = nullptr;       // [2][B][C] slots in (last_used, slot) order, by step parity
   uint16_t* pool = nullptr;       // [B][C][D] bf16
   long long* stats = nullptr;     // [kStatFields]
 };
@@ -60,7 +62,8 @@ struct Scratch {
   int32_t* miss_tok = nullptr;    // [B][M*k]
   int32_t* miss_slot = nullptr;   // [B][M*k]
   int32_t* n_miss = nullptr;      // [B]
-  unsigned long long* vict = nullptr;  // [B][M*k]
+  int32_t* vlist = nullptr;       // [B][M*k] victims in LRU order
+  uint32_t* ghist = nullptr;      // [B][M][kHistBins] score histogram
   float* part_o = nullptr;        // [B][M][nch][H][512]
   float2* part_ml = nullptr;      // [B][M][nch][H]
   uint8_t* h_qidx = nullptr;      // staging for ess_step_host
@@ -75,9 +78,9 @@ struct Layout {
   size_t total = 0;
   size_t layer_bytes = 0;
   // per layer (relative to the layer base)
-  size_t o_T, o_tiles, o_cslots, o_stoken, o_lused, o_step, o_pool, o_stats;
+  size_t o_T, o_tiles, o_cslots, o_stoken, o_lused, o_step, o_pool, o_stats, o_order;
   // scratch (absolute)
-  size_t o_scores, o_tidx, o_tslot, o_nmw, o_mtok, o_mslot, o_nmiss, o_vict, o_po, o_pml,
+  size_t o_scores, o_tidx, o_tslot, o_nmw, o_mtok, o_mslot, o_nmiss, o_vict, o_hist, o_po, o_pml,
       o_hq, o_hw, o_hqm, o_hout, o_status;
   int nch = 0;                    // attention chunks per (request, way)
 };
@@ -98,11 +101,15 @@ struct ess_pool {
 namespace ess {
 
 // Kernel launchers (one per kernel file).  They assume validated arguments.
+// with_hist: also accumulate the per-(request, way) score histogram in the
+// pool's scratch (it must be zero; the selection kernel zeroes it after use).
 cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, const float* w,
-                           float* scores, cudaStream_t st);
-cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, int32_t* topk_idx,
-                          int32_t* topk_slot, int32_t* n_miss_way, int32_t* miss_tok,
-                          int32_t* miss_slot, int32_t* n_miss, cudaStream_t st);
+                           float* scores, bool with_hist, cudaStream_t st);
+// hist_given: the indexer filled the histogram; otherwise the kernel builds it.
+cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, bool hist_given,
+                          int32_t* topk_idx, int32_t* topk_slot, int32_t* n_miss_way,
+                          int32_t* miss_tok, int32_t* miss_slot, int32_t* n_miss, cudaStream_t st);
+cudaError_t launch_order_reset(const ess_pool& p, int layer, cudaStream_t st);
 cudaError_t launch_stage(const ess_pool& p, int layer, const int32_t* miss_tok,
                          const int32_t* miss_slot, const int32_t* n_miss, cudaStream_t st);
 cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,

@@ -12,16 +12,31 @@
 //    slots; loads equal evictions so |C_b| never changes;
 //  - LIM emits the top-k slot list and copy triples (DRAM source, HBM
 //    destination, count) and puts the misses at the head of the list.
+//  Once a CTA knows which of its tokens miss, it asks L2 to prefetch their
+//  host rows, so the host-link transfer (and the GPU's first translation of
+//  those host pages) overlaps the LRU bookkeeping that follows.
 // "ESS: Latent-Cache Offload": the GPU sparse pool keeps its hot subset
 // under LRU.
 //
 // One cluster of kSelCluster CTAs handles one request; CTA r owns tokens
-// [r*n_local, (r+1)*n_local) and slots [r*c_local, (r+1)*c_local).  The top-k
-// threshold is found exactly by MSB-first radix passes whose per-CTA
-// histograms are summed through distributed shared memory; ties at the
-// threshold go to the lowest token (lowest slot for victims).  All lists
-// come out in ascending token order, which fixes the pairing of the i-th
-// miss with the i-th victim in (last_used, slot) order.
+// [r*n_local, (r+1)*n_local) and positions/slots [r*c_local, (r+1)*c_local).
+//
+// Top-k: a histogram of the top 12 bits of the order-preserving score keys
+// (filled by the indexer, or built here for caller scores) gives the bin
+// that holds the k-th largest score.  One ordered pass lists the tokens
+// above that bin (selected) and in it (candidates); MSB radix passes over
+// the candidates' low 20 bits, with per-CTA histograms summed through
+// distributed shared memory, fix the exact threshold; equal keys go to the
+// lowest token.  If the candidates could overflow the list, the kernel
+// falls back to radix passes over every token.  All lists come out in
+// ascending token order.
+//
+// LRU: the slots are kept in a list sorted by (last_used, slot), double
+// buffered by step parity.  After the hits are stamped, the unstamped
+// entries in list order are exactly the eviction order, so the first
+// |Miss| of them are the victims, already in the order that pairs the i-th
+// miss with the i-th victim; the next list is the remaining unstamped
+// entries followed by the stamped slots in slot order.
 #include "ess_device.cuh"
 
 namespace ess {
@@ -31,12 +46,19 @@ constexpr int CL = kSelCluster;
 constexpr int NT = kSelThreads;
 constexpr int NW = NT / 32;
 
+
+constexpr int kDigBits = 10;               // radix digit width of the exact passes
+constexpr int kDig = 1 << kDigBits;
+
 struct SelArgs {
   const float* scores;        // [B][M][T]
+  uint32_t* ghist;            // [B][M][kHistBins]
+  int hist_given;             // 1: filled by the indexer; 0: build it here
   int32_t* cache_slots;       // [B][T]
   int32_t* slot_token;        // [B][C]
   int32_t* last_used;         // [B][C]
   int32_t* step;              // [B]
+  int32_t* order;             // [2][B][C]
   const int32_t* Tb;          // [B]
   int32_t* topk_idx;          // [B][M][k]
   int32_t* topk_slot;         // [B][M][k]
@@ -44,36 +66,44 @@ struct SelArgs {
   int32_t* miss_tok;          // [B][M*k]
   int32_t* miss_slot;         // [B][M*k]
   int32_t* n_miss;            // [B]
-  unsigned long long* vict;   // [B][M*k]
+  int32_t* vlist;             // [B][M*k] victims in LRU order
+  const uint16_t* host;       // [B][T][576] host rows (device alias), for the miss prefetch
+  const int32_t* page_table;  // [B][T/page] or null
+  int page;
   long long* stats;           // [kStatFields]
   int* status;
   int B, M, k, T, C;
   int n_local;                // tokens per CTA (multiple of 4)
-  int c_local;                // slots per CTA
+  int c_local;                // slots / order positions per CTA
   int resident;               // scores staged in shared memory
-  int ucap;                   // union-list capacity per CTA
-  uint32_t keys_bytes;        // size of the keys / sort region
+  int lcap;                   // token-list capacity per CTA
+  int gcap;                   // gathered-candidate capacity per CTA
+  uint32_t keys_bytes;        // size of the staged-scores region
 };
 
 struct SelShared {
-  uint32_t hist[2][kMaxWays * 256];
-  uint32_t tot[kMaxWays * 256];
+  uint32_t hist[2][kMaxWays * kDig];
+  uint32_t tot[kMaxWays * kDig];
   int scanbuf[2][NW];
+  int wcount[NW];
   uint32_t prefix[kMaxWays], selmask[kMaxWays];
   int remaining[kMaxWays], eq_local[kMaxWays], eq_before[kMaxWays], eq_total[kMaxWays];
-  int active[kMaxWays], quota[kMaxWays], rank_needed[kMaxWays], eq_run[kMaxWays];
+  int active[kMaxWays], quota[kMaxWays], rank_needed[kMaxWays];
   int last_lo, last_dmask;
-  int nu;
+  int b1[kMaxWays], take1[kMaxWays], cand1[kMaxWays];  // coarse threshold bin per way
+  int fallback;
+  int nl;
+  int ncand[kMaxWays];                // this CTA's candidates per way (read through DSMEM)
+  int gsel;                           // 1: candidates are gathered into every CTA
   // published for the other CTAs of the cluster (read through DSMEM)
-  int pub_nmiss, pub_nu, pub_hit[kMaxWays], pub_miss[kMaxWays];
-  int pub_lumin, pub_lumax, pub_vcnt;
+  int pub_overflow, pub_nmiss, pub_nu, pub_hit[kMaxWays], pub_miss[kMaxWays], pub_unst,
+      pub_stamp;
   // cluster-wide values derived from the publications
   int n_miss_total, nu_total, miss_off, hit_off[kMaxWays], wmiss_off[kMaxWays], nmw[kMaxWays];
   int hits_total[kMaxWays];
-  int lu_min, lu_max, vict_off;
+  int unst_before, unst_total, stamp_before;
   int step_b;
   unsigned long long bar;
-  int abort;
 };
 
 __device__ __forceinline__ void hist_add_warp(uint32_t* h, uint32_t bin, bool ok) {
@@ -110,26 +140,58 @@ __device__ __forceinline__ int block_scan(int v, int& tot, SelShared& sh, int& p
   return pre + x - v;
 }
 
+// Ordered positions for a block-wide compaction (same `run` in every thread).
+__device__ __forceinline__ int ordered_pos(int v, int& run, SelShared& sh, int& parity) {
+  int tot;
+  const int p = run + block_scan(v, tot, sh, parity);
+  run += tot;
+  return p;
+}
+
+// Exclusive prefix of per-warp counts (one __syncthreads; callers keep the
+// wcount buffer free until every thread has passed the next barrier).
+__device__ __forceinline__ int warp_base(int wcnt, int& total, SelShared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) sh.wcount[warp] = wcnt;
+  __syncthreads();
+  int pre = 0, t = 0;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    const int u = sh.wcount[i];
+    pre += (i < warp) ? u : 0;
+    t += u;
+  }
+  total = t;
+  return pre;
+}
+
+// Sum of a shared-memory word over the CTAs of the cluster (and over ranks
+// below upto_rank).
 __device__ __forceinline__ uint32_t sum_over_cluster(const void* local, uint32_t upto_rank,
                                                      uint32_t* before) {
   const uint32_t a = smem_u32(local);
+  uint32_t v[CL];
+#pragma unroll
+  for (uint32_t r = 0; r < CL; ++r) v[r] = ld_dsmem_u32(dsmem_addr(a, r));
   uint32_t s = 0, b = 0;
+#pragma unroll
   for (uint32_t r = 0; r < CL; ++r) {
-    const uint32_t v = ld_dsmem_u32(dsmem_addr(a, r));
-    if (r < upto_rank) b += v;
-    s += v;
+    if (r < upto_rank) b += v[r];
+    s += v[r];
   }
   if (before) *before = b;
   return s;
 }
 
 // Cluster-wide exact selection of the remaining[m] largest keys (keys <
-// 2^nbits) per active way; elements of rank r precede those of rank r+1, and
-// equal keys go to the lowest element.  Leaves prefix[m] (threshold key),
-// remaining[m] (how many threshold-equal elements to take, lowest first) and
-// eq_local / eq_before / eq_total of threshold-equal elements.
-// Precondition: a cluster_sync separates this call from any earlier remote
-// read of sh.hist.
+// 2^nbits) per active way over the elements for which keyf(m, i, key) is
+// true; elements of rank r precede those of rank r+1, and equal keys go to
+// the lowest element.  MSB-first passes of kDigBits-bit digits; per-CTA
+// histograms are summed through distributed shared memory.  Leaves prefix[m]
+// (threshold key), remaining[m] (how many threshold-equal elements to take,
+// lowest first) and eq_local / eq_before / eq_total of threshold-equal
+// elements.  Precondition: a cluster_sync separates this call from any
+// earlier remote read of sh.hist.
 template <class KeyFn>
 __device__ void cluster_select(KeyFn keyf, int n_valid, int nw, int nbits, SelShared& sh,
                                uint32_t rank) {
@@ -138,44 +200,42 @@ __device__ void cluster_select(KeyFn keyf, int n_valid, int nw, int nbits, SelSh
     sh.prefix[tid] = 0;
     sh.selmask[tid] = 0;
   }
-  for (int i = tid; i < 2 * kMaxWays * 256; i += NT) (&sh.hist[0][0])[i] = 0;
+  for (int i = tid; i < 2 * kMaxWays * kDig; i += NT) (&sh.hist[0][0])[i] = 0;
   __syncthreads();
-  const int passes = (nbits + 7) / 8;
+  const int passes = (nbits + kDigBits - 1) / kDigBits;
   for (int p = 0; p < passes; ++p) {
-    const int hi = nbits - 8 * p;
-    const int lo = hi - 8 > 0 ? hi - 8 : 0;
-    const uint32_t dmask = (hi - lo >= 32) ? 0xffffffffu : ((1u << (hi - lo)) - 1u);
+    const int hi = nbits - kDigBits * p;
+    const int lo = hi - kDigBits > 0 ? hi - kDigBits : 0;
+    const uint32_t dmask = (1u << (hi - lo)) - 1u;
     uint32_t* H = sh.hist[p & 1];
     for (int m = 0; m < nw; ++m) {
       if (!sh.active[m]) continue;
       const uint32_t pre = sh.prefix[m], msk = sh.selmask[m];
       for (int base = 0; base < n_valid; base += NT) {
         const int i = base + tid;
-        bool ok = i < n_valid;
-        const uint32_t key = ok ? keyf(m, i) : 0u;
+        uint32_t key = 0u;
+        bool ok = i < n_valid && keyf(m, i, key);
         ok = ok && ((key & msk) == pre);
-        hist_add_warp(H + m * 256, (key >> lo) & dmask, ok);
+        hist_add_warp(H + m * kDig, (key >> lo) & dmask, ok);
       }
     }
     __syncthreads();
     cluster_sync();
-    for (int i = tid; i < nw * 256; i += NT) {
-      if (!sh.active[i >> 8]) continue;
+    for (int i = tid; i < nw * kDig; i += NT) {
+      if (!sh.active[i / kDig]) continue;
       sh.tot[i] = sum_over_cluster(&H[i], 0, nullptr);
     }
     __syncthreads();
     const int warp = tid >> 5, lane = tid & 31;
     if (warp < nw && sh.active[warp]) {
+      // lane l covers bins kDig-1-32l-j, j = 0..31 (descending)
       const int m = warp;
       const int need = sh.remaining[m];
-      int c8[8];
-      int s8 = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c8[j] = static_cast<int>(sh.tot[m * 256 + 255 - 8 * lane - j]);
-        s8 += c8[j];
-      }
-      int incl = s8;
+      const uint32_t* T = sh.tot + m * kDig + kDig - 1 - 32 * lane;
+      int s32 = 0;
+#pragma unroll 8
+      for (int j = 0; j < 32; ++j) s32 += static_cast<int>(T[-j]);
+      int incl = s32;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -184,13 +244,15 @@ __device__ void cluster_select(KeyFn keyf, int n_valid, int nw, int nbits, SelSh
       const unsigned bal = __ballot_sync(0xffffffffu, incl >= need);
       const int L = bal ? __ffs(bal) - 1 : 31;
       if (lane == L) {
-        int acc = incl - s8;
+        const uint32_t* TL = sh.tot + m * kDig + kDig - 1 - 32 * L;
+        int acc = incl - s32;
         int j = 0;
-        for (; j < 7; ++j) {
-          if (acc + c8[j] >= need) break;
-          acc += c8[j];
+        for (; j < 31; ++j) {
+          const int cj = static_cast<int>(TL[-j]);
+          if (acc + cj >= need) break;
+          acc += cj;
         }
-        const uint32_t digit = static_cast<uint32_t>(255 - 8 * L - j);
+        const uint32_t digit = static_cast<uint32_t>(kDig - 1 - 32 * L - j);
         sh.prefix[m] |= digit << lo;
         sh.selmask[m] |= dmask << lo;
         sh.remaining[m] = need - acc;
@@ -202,13 +264,13 @@ __device__ void cluster_select(KeyFn keyf, int n_valid, int nw, int nbits, SelSh
     }
     __syncthreads();
     if (p + 1 < passes)
-      for (int i = tid; i < kMaxWays * 256; i += NT) sh.hist[(p + 1) & 1][i] = 0;
+      for (int i = tid; i < kMaxWays * kDig; i += NT) sh.hist[(p + 1) & 1][i] = 0;
     __syncthreads();
   }
   if (passes > 0 && tid < nw && sh.active[tid]) {
     const int m = tid;
     const uint32_t dig = (sh.prefix[m] >> sh.last_lo) & static_cast<uint32_t>(sh.last_dmask);
-    const uint32_t* h = &sh.hist[(passes - 1) & 1][m * 256 + dig];
+    const uint32_t* h = &sh.hist[(passes - 1) & 1][m * kDig + dig];
     uint32_t before = 0;
     const uint32_t total = sum_over_cluster(h, rank, &before);
     sh.eq_local[m] = static_cast<int>(*h);
@@ -227,7 +289,6 @@ __device__ __forceinline__ void set_quota(SelShared& sh, int nw) {
     q = q < 0 ? 0 : (q > sh.eq_local[m] ? sh.eq_local[m] : q);
     sh.quota[m] = q;
     sh.rank_needed[m] = (q > 0 && q < sh.eq_local[m]) ? 1 : 0;
-    sh.eq_run[m] = 0;
   }
 }
 
@@ -236,6 +297,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   extern __shared__ __align__(16) uint8_t dsm[];
   __shared__ SelShared sh;
   const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
   const int b = blockIdx.x / CL;
   const int M = a.M;
@@ -245,25 +307,30 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   const int r0 = static_cast<int>(rank) * a.n_local;
   int nloc = Tb - r0;
   nloc = nloc < 0 ? 0 : (nloc > a.n_local ? a.n_local : nloc);
-  float* keys_s = reinterpret_cast<float*>(dsm);                        // [M][n_local] or sort buffer
-  int* lu_s = reinterpret_cast<int*>(dsm + a.keys_bytes);               // [c_local]
-  int* utok = lu_s + a.c_local;                                         // [ucap]
-  int* uslot = utok + a.ucap;                                           // [ucap]
-  uint8_t* umask = reinterpret_cast<uint8_t*>(uslot + a.ucap);          // [ucap]
+  float* keys_s = reinterpret_cast<float*>(dsm);                      // [M][n_local]
+  int* ltok = reinterpret_cast<int*>(dsm + a.keys_bytes);             // [lcap] token list
+  int* lslot = ltok + a.lcap;                                         // [lcap] resolved slot
+  int* cslot = lslot + a.lcap;                                        // [c_local] list prefetch
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(cslot + a.c_local);    // [M][lcap] candidate keys
+  uint32_t* gkey = ckey + M * a.lcap;                                 // [gcap] gathered keys
+  uint8_t* grank = reinterpret_cast<uint8_t*>(gkey + a.gcap);         // [gcap] source rank
+  uint8_t* lflag = grank + a.gcap;                                    // [lcap] way bits
+  uint8_t* cflag = lflag + a.lcap;                                    // [c_local]
+  const int n_local = a.n_local, lcap = a.lcap, Tmax = a.T;
+  const bool resident = a.resident != 0;
   const size_t bT = static_cast<size_t>(b) * a.T;
   const size_t bC = static_cast<size_t>(b) * a.C;
+  uint32_t* gh = a.ghist + static_cast<size_t>(b) * M * kHistBins;
+  const unsigned lt = lanemask_lt();
   int parity = 0;
 
   if (tid == 0) {
-    sh.step_b = a.step[b];
-    sh.nu = 0;
-    sh.abort = 0;
-    sh.pub_nmiss = 0;
-    sh.pub_nu = 0;
-    sh.pub_vcnt = 0;
+    sh.step_b = a.step[b];  // (also read directly as step0)
+    sh.nl = 0;
+    sh.fallback = 0;
+    sh.pub_overflow = sh.pub_nmiss = sh.pub_nu = sh.pub_unst = sh.pub_stamp = 0;
     for (int m = 0; m < kMaxWays; ++m) {
-      sh.pub_hit[m] = 0;
-      sh.pub_miss[m] = 0;
+      sh.pub_hit[m] = sh.pub_miss[m] = 0;
       sh.active[m] = 0;
     }
     mbar_init(smem_u32(&sh.bar), 1);
@@ -271,80 +338,347 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   }
   __syncthreads();
 
+  // this CTA's positions of the current LRU list (read after the hits are stamped)
+  const int step0 = a.step[b];
+  const int p0 = static_cast<int>(rank) * a.c_local;
+  int cl = a.C - p0;
+  cl = cl < 0 ? 0 : (cl > a.c_local ? a.c_local : cl);
+  const int32_t* ocur = a.order + (static_cast<size_t>(step0 & 1) * a.B + b) * a.C;
+  int32_t* onxt = a.order + (static_cast<size_t>((step0 & 1) ^ 1) * a.B + b) * a.C;
+
   // ---------------------------------------------------------------- scores
-  if (a.resident && nloc > 0) {
-    const int cnt = ((nloc + 3) / 4) * 4 <= a.T - r0 ? ((nloc + 3) / 4) * 4 : a.T - r0;
-    if (tid == 0) {
-      mbar_arrive_expect_tx(smem_u32(&sh.bar), static_cast<uint32_t>(cnt * 4 * M));
-      for (int m = 0; m < M; ++m)
-        bulk_load(smem_u32(keys_s + m * a.n_local),
-                  a.scores + (static_cast<size_t>(b) * M + m) * a.T + r0,
-                  static_cast<uint32_t>(cnt * 4), smem_u32(&sh.bar));
+  {
+    const int cnt = ((nloc + 3) / 4) * 4 <= Tmax - r0 ? ((nloc + 3) / 4) * 4 : Tmax - r0;
+    const bool load_scores = resident && nloc > 0;
+    // the order list slice is copied in 16-byte units when aligned, else by threads
+    const bool bulk_order = cl > 0 && (cl & 3) == 0 && (p0 & 3) == 0 && (a.C & 3) == 0;
+    if (tid == 0 && (load_scores || bulk_order)) {
+      uint32_t bytes = (load_scores ? cnt * 4 * M : 0) + (bulk_order ? cl * 4 : 0);
+      mbar_arrive_expect_tx(smem_u32(&sh.bar), bytes);
+      if (load_scores)
+        for (int m = 0; m < M; ++m)
+          bulk_load(smem_u32(keys_s + m * n_local),
+                    a.scores + (static_cast<size_t>(b) * M + m) * Tmax + r0,
+                    static_cast<uint32_t>(cnt * 4), smem_u32(&sh.bar));
+      if (bulk_order)
+        bulk_load(smem_u32(cslot), ocur + p0, static_cast<uint32_t>(cl * 4), smem_u32(&sh.bar));
     }
-    if (!mbar_wait(smem_u32(&sh.bar), 0, nullptr)) {
+    if (!bulk_order)
+      for (int i = tid; i < cl; i += NT) cslot[i] = ocur[p0 + i];
+    if ((load_scores || bulk_order) && !mbar_wait(smem_u32(&sh.bar), 0, nullptr))
       set_status(a.status, ESS_ERR_TIMEOUT);
-      sh.abort = 1;
-    }
+    __syncthreads();
   }
-  const float* gscores = a.scores + static_cast<size_t>(b) * M * a.T + r0;
-  auto score_key = [&](int m, int i) -> uint32_t {
-    const float f = a.resident ? keys_s[m * a.n_local + i] : gscores[static_cast<size_t>(m) * a.T + i];
-    return float_key(f);
+  const float* gscores = a.scores + static_cast<size_t>(b) * M * Tmax + r0;
+  auto score_key = [=](int m, int i) -> uint32_t {
+    const float f = resident ? keys_s[m * n_local + i] : gscores[static_cast<size_t>(m) * Tmax + i];
+    return float_key(f + 0.0f);  // +0 and -0 compare equal, as scores do
   };
 
   // ---------------------------------------------------------------- (a2) top-k
   const bool sel_all = keff >= Tb;  // every token is selected (includes T_b = 0)
-  if (tid < M) {
-    sh.active[tid] = sel_all ? 0 : 1;
-    sh.remaining[tid] = keff;
+  if (!sel_all && !a.hist_given) {
+    // caller scores: build the 12-bit histogram of this request
+    for (int m = 0; m < M; ++m)
+      for (int base = 0; base < nloc; base += NT) {
+        const int i = base + tid;
+        const bool ok = i < nloc;
+        hist_add_warp(gh + m * kHistBins, ok ? score_key(m, i) >> 20 : 0u, ok);
+      }
+    __syncthreads();
+    cluster_sync();
   }
-  __syncthreads();
   if (!sel_all) {
-    cluster_select(score_key, nloc, M, 32, sh, rank);
-    set_quota(sh, M);
+    for (int m = 0; m < M; ++m) {
+      // thread t owns bins 4095 - 8t - j, j = 0..7 (descending order)
+      int c8[8];
+      int s8 = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c8[j] = static_cast<int>(gh[m * kHistBins + kHistBins - 1 - 8 * tid - j]);
+        s8 += c8[j];
+      }
+      int tot;
+      const int excl = block_scan(s8, tot, sh, parity);
+      if (excl < keff && keff <= excl + s8) {
+        int acc = excl, j = 0;
+        for (; j < 7; ++j) {
+          if (acc + c8[j] >= keff) break;
+          acc += c8[j];
+        }
+        sh.b1[m] = kHistBins - 1 - 8 * tid - j;
+        sh.take1[m] = keff - acc;
+        sh.cand1[m] = c8[j];
+      }
+      if (tid == 0 && tot != Tb) sh.fallback = 1;  // histogram does not describe these scores
+    }
     __syncthreads();
   }
-  // ordered compaction of the union of the ways' selections into utok/umask
-  {
+  bool fast = !sel_all && !sh.fallback;
+  if (sel_all) {
+    for (int i = tid; i < nloc; i += NT) {
+      ltok[i] = r0 + i;
+      lflag[i] = static_cast<uint8_t>((1u << M) - 1u);
+    }
+    if (tid == 0) sh.nl = nloc;
+    __syncthreads();
+  }
+  if (fast) {
+    // one ordered pass over this CTA's tokens, each warp over its own
+    // contiguous range: tokens above the coarse bin are selected (low
+    // nibble), tokens in it are candidates (high nibble)
+    uint32_t lo_k[kMaxWays], hi_k[kMaxWays];
+#pragma unroll
+    for (int m = 0; m < kMaxWays; ++m) {
+      const bool use = m < M;
+      const uint32_t bin = use ? static_cast<uint32_t>(sh.b1[m]) : 0xFFFu;
+      const bool all_in = use && sh.take1[m] == sh.cand1[m];
+      lo_k[m] = bin << 20;                                    // key >= lo: at or above the bin
+      hi_k[m] = all_in ? (bin << 20) : ((bin + 1u) << 20);    // key >= hi: selected outright
+      if (!use) lo_k[m] = hi_k[m] = 0xFFFFFFFFu;
+      if (use && bin == 0xFFFu && !all_in) hi_k[m] = 0xFFFFFFFFu;  // top bin: nothing above it
+    }
+    auto coarse_flags = [&](int i) -> uint32_t {
+      uint32_t f = 0;
+#pragma unroll
+      for (int m = 0; m < kMaxWays; ++m) {
+        if (m >= M) break;
+        const uint32_t key = score_key(m, i);
+        if (key >= hi_k[m]) f |= 1u << m;
+        else if (key >= lo_k[m]) f |= 16u << m;
+      }
+      return f;
+    };
+    const int per_w = (((nloc + NW - 1) / NW) + 31) & ~31;
+    const int wlo = warp * per_w;
+    const int whi = wlo + per_w < nloc ? wlo + per_w : nloc;
+    int wcnt = 0;
+    for (int base = wlo; base < whi; base += 32) {
+      const int i = base + lane;
+      const uint32_t f = i < whi ? coarse_flags(i) : 0u;
+      wcnt += __popc(__ballot_sync(0xffffffffu, f != 0));
+    }
+    int total;
+    int pos = warp_base(wcnt, total, sh);
+    for (int base = wlo; base < whi; base += 32) {
+      const int i = base + lane;
+      const uint32_t f = i < whi ? coarse_flags(i) : 0u;
+      const unsigned bal = __ballot_sync(0xffffffffu, f != 0);
+      if (f) {
+        const int p = pos + __popc(bal & lt);
+        if (p < lcap) {
+          ltok[p] = r0 + i;
+          lflag[p] = static_cast<uint8_t>(f);
+        }
+      }
+      pos += __popc(bal);
+    }
+    const int nl = total < lcap ? total : lcap;
+    // candidates of each way in list order, with their low 20 key bits
+    if (tid < M) {
+      sh.active[tid] = sh.take1[tid] < sh.cand1[tid] ? 1 : 0;
+      sh.remaining[tid] = sh.take1[tid];
+    }
+    __syncthreads();
+    for (int m = 0; m < M; ++m) {
+      if (!sh.active[m]) {
+        if (tid == 0) sh.ncand[m] = 0;
+        continue;
+      }
+      int run = 0;
+      for (int base = 0; base < nl; base += NT) {
+        const int e = base + tid;
+        const bool c = e < nl && (lflag[e] & (16u << m));
+        const int p = ordered_pos(c ? 1 : 0, run, sh, parity);
+        if (c) ckey[m * lcap + p] = score_key(m, ltok[e] - r0) & 0xFFFFFu;
+      }
+      if (tid == 0) sh.ncand[m] = run;
+    }
+    if (tid == 0) {
+      sh.nl = nl;
+      sh.pub_overflow = total > lcap ? 1 : 0;
+      int need = 0;
+      for (int m = 0; m < M; ++m) need += sh.active[m] ? sh.cand1[m] : 0;
+      sh.gsel = need <= a.gcap ? 1 : 0;   // same in every CTA: from the shared histogram
+    }
+    __syncthreads();
+    cluster_sync();  // lists and candidate keys complete; overflow flags published
+    if (tid == 0)
+      sh.fallback = sum_over_cluster(&sh.pub_overflow, 0, nullptr) ? 1 : 0;
+    __syncthreads();
+    fast = !sh.fallback;
+  }
+  if (fast) {
+    const int nl = sh.nl;
+    bool any = false;
+    for (int m = 0; m < M; ++m) any |= sh.active[m] != 0;
+    if (any && sh.gsel) {
+      // gather every CTA's candidate keys (in cluster order) and find the
+      // exact threshold locally: the same result in every CTA, no more barriers
+      for (int m = 0; m < M; ++m) {
+        if (!sh.active[m]) continue;
+        int off = 0;
+        for (uint32_t r = 0; r < CL; ++r) {
+          const int n = static_cast<int>(ld_dsmem_u32(dsmem_addr(smem_u32(&sh.ncand[m]), r)));
+          const uint32_t src = dsmem_addr(smem_u32(ckey + m * lcap), r);
+          for (int i = tid; i < n && off + i < a.gcap; i += NT) {
+            gkey[off + i] = ld_dsmem_u32(src + 4u * i);
+            grank[off + i] = static_cast<uint8_t>(r);
+          }
+          off += n;
+        }
+        __syncthreads();
+        const int ng = off < a.gcap ? off : a.gcap;
+        // exact take1-th largest of the gathered keys: two 10-bit passes
+        uint32_t* H = sh.hist[0];
+        uint32_t pre = 0, msk = 0;
+        int need = sh.remaining[m];
+        for (int p = 0; p < 2; ++p) {
+          const int lo = p == 0 ? 10 : 0;
+          for (int i = tid; i < kDig; i += NT) H[i] = 0;
+          __syncthreads();
+          for (int i = tid; i < ng; i += NT) {
+            const uint32_t k = gkey[i];
+            if ((k & msk) == pre) atomicAdd(&H[(k >> lo) & (kDig - 1)], 1u);
+          }
+          __syncthreads();
+          if (warp == 0) {
+            const uint32_t* T = H + kDig - 1 - 32 * lane;
+            int s32 = 0;
+            for (int j = 0; j < 32; ++j) s32 += static_cast<int>(T[-j]);
+            int incl = s32;
+            for (int o = 1; o < 32; o <<= 1) {
+              const int y = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += y;
+            }
+            const unsigned bal = __ballot_sync(0xffffffffu, incl >= need);
+            const int L = bal ? __ffs(bal) - 1 : 31;
+            if (lane == L) {
+              const uint32_t* TL = H + kDig - 1 - 32 * L;
+              int acc = incl - s32, j = 0;
+              for (; j < 31; ++j) {
+                const int cj = static_cast<int>(TL[-j]);
+                if (acc + cj >= need) break;
+                acc += cj;
+              }
+              sh.prefix[m] = pre | (static_cast<uint32_t>(kDig - 1 - 32 * L - j) << lo);
+              sh.remaining[m] = need - acc;
+            }
+          }
+          __syncthreads();
+          pre = sh.prefix[m];
+          msk |= static_cast<uint32_t>(kDig - 1) << lo;
+          need = sh.remaining[m];
+          __syncthreads();
+        }
+        // threshold-equal candidates: this CTA's count and those of lower ranks
+        if (tid == 0) {
+          sh.eq_local[m] = 0;
+          sh.eq_before[m] = 0;
+        }
+        __syncthreads();
+        int el = 0, eb = 0;
+        for (int i = tid; i < ng; i += NT) {
+          if (gkey[i] != pre) continue;
+          const uint32_t r = grank[i];
+          el += r == rank ? 1 : 0;
+          eb += r < rank ? 1 : 0;
+        }
+        for (int o = 16; o; o >>= 1) {
+          el += __shfl_xor_sync(0xffffffffu, el, o);
+          eb += __shfl_xor_sync(0xffffffffu, eb, o);
+        }
+        if (lane == 0 && (el || eb)) {
+          atomicAdd(&sh.eq_local[m], el);
+          atomicAdd(&sh.eq_before[m], eb);
+        }
+        __syncthreads();
+      }
+      set_quota(sh, M);
+      __syncthreads();
+    } else if (any) {
+      auto cand_key = [&](int m, int e, uint32_t& key) -> bool {
+        if (!(lflag[e] & (16u << m))) return false;
+        key = score_key(m, ltok[e] - r0) & 0xFFFFFu;
+        return true;
+      };
+      cluster_select(cand_key, nl, M, 20, sh, rank);
+      set_quota(sh, M);
+      __syncthreads();
+    }
+    // filter the list in place into the union of the ways' selections
+    int eqrun[kMaxWays] = {0, 0, 0, 0};
     int nu = 0;
-    int eqrun[kMaxWays] = {0, 0, 0, 0};  // threshold-equal elements seen so far (same in all threads)
+    for (int base = 0; base < nl; base += NT) {
+      const int e = base + tid;
+      int tok = 0;
+      uint32_t f = 0;
+      if (e < nl) {
+        tok = ltok[e];
+        f = lflag[e];
+      }
+      uint32_t sel = f & 0xFu;
+      for (int m = 0; m < M; ++m) {
+        if (!sh.active[m]) continue;
+        const bool cm = (f >> (4 + m)) & 1u;
+        const uint32_t k20 = cm ? (score_key(m, tok - r0) & 0xFFFFFu) : 0u;
+        const uint32_t thr = sh.prefix[m];
+        const bool eq = cm && k20 == thr;
+        if (cm && k20 > thr) sel |= 1u << m;
+        if (sh.rank_needed[m]) {
+          const int r = ordered_pos(eq ? 1 : 0, eqrun[m], sh, parity);
+          if (eq && r < sh.quota[m]) sel |= 1u << m;
+        } else if (eq && sh.quota[m] > 0) {
+          sel |= 1u << m;
+        }
+      }
+      const int pos = ordered_pos(sel ? 1 : 0, nu, sh, parity);
+      if (sel) {
+        ltok[pos] = tok;
+        lflag[pos] = static_cast<uint8_t>(sel);
+      }
+    }
+    if (tid == 0) sh.nl = nu;
+    __syncthreads();
+  } else if (!sel_all) {
+    // fallback: exact radix passes over every token
+    if (tid < M) {
+      sh.active[tid] = 1;
+      sh.remaining[tid] = keff;
+    }
+    __syncthreads();
+    auto all_key = [&](int m, int i, uint32_t& key) -> bool {
+      key = score_key(m, i);
+      return true;
+    };
+    cluster_select(all_key, nloc, M, 32, sh, rank);
+    set_quota(sh, M);
+    __syncthreads();
+    int eqrun[kMaxWays] = {0, 0, 0, 0};
+    int nu = 0;
     for (int base = 0; base < nloc; base += NT * 4) {
       const int i0 = base + tid * 4;
       uint32_t selbits[4] = {0, 0, 0, 0};
       for (int m = 0; m < M; ++m) {
-        uint32_t key[4];
-        bool valid[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          valid[j] = (i0 + j) < nloc;
-          key[j] = valid[j] ? score_key(m, i0 + j) : 0u;
-        }
-        if (sel_all) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (valid[j]) selbits[j] |= 1u << m;
-          continue;
-        }
         const uint32_t thr = sh.prefix[m];
         bool eq[4];
         int neq = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          eq[j] = valid[j] && key[j] == thr;
+          const bool valid = (i0 + j) < nloc;
+          const uint32_t key = valid ? score_key(m, i0 + j) : 0u;
+          eq[j] = valid && key == thr;
           neq += eq[j];
-          if (valid[j] && key[j] > thr) selbits[j] |= 1u << m;
+          if (valid && key > thr) selbits[j] |= 1u << m;
         }
-        if (sh.rank_needed[m]) {  // uniform
-          int tot;
-          int r = block_scan(neq, tot, sh, parity);
-          r += eqrun[m];
+        if (sh.rank_needed[m]) {
+          int r = ordered_pos(neq, eqrun[m], sh, parity);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             if (eq[j]) {
               if (r < sh.quota[m]) selbits[j] |= 1u << m;
               ++r;
             }
-          eqrun[m] += tot;
         } else if (sh.quota[m] > 0) {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -354,45 +688,42 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       int cu = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) cu += selbits[j] ? 1 : 0;
-      int tot;
-      int pos = nu + block_scan(cu, tot, sh, parity);
+      int pos = ordered_pos(cu, nu, sh, parity);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         if (selbits[j]) {
-          if (pos < a.ucap) {
-            utok[pos] = r0 + i0 + j;
-            umask[pos] = static_cast<uint8_t>(selbits[j]);
+          if (pos < a.lcap) {
+            ltok[pos] = r0 + i0 + j;
+            lflag[pos] = static_cast<uint8_t>(selbits[j]);
           } else {
             set_status(a.status, ESS_ERR_DEVICE_CHECK);
           }
           ++pos;
         }
-      nu += tot;
     }
-    if (tid == 0) sh.nu = nu < a.ucap ? nu : a.ucap;
+    if (tid == 0) sh.nl = nu < a.lcap ? nu : a.lcap;
     __syncthreads();
   }
-  const int nu = sh.nu;
+  const int nu = sh.nl;
 
   // ---------------------------------------------------------------- (a3) resolve
   for (int e = tid; e < nu; e += NT) {
-    const int t = utok[e];
+    const int t = ltok[e];
     int s = a.cache_slots[bT + t];
     if (s >= a.C || s < -1) {
       set_status(a.status, ESS_ERR_DEVICE_CHECK);
       s = -1;
     }
-    uslot[e] = s;
+    lslot[e] = s;
     if (s >= 0) a.last_used[bC + s] = sh.step_b;   // hits are stamped first
-    const uint32_t mk = umask[e];
+    const uint32_t mk = lflag[e];
     for (int m = 0; m < M; ++m)
       if (mk & (1u << m)) atomicAdd(s >= 0 ? &sh.pub_hit[m] : &sh.pub_miss[m], 1);
     if (s < 0) atomicAdd(&sh.pub_nmiss, 1);
   }
   if (tid == 0) sh.pub_nu = nu;
-  __threadfence();
   __syncthreads();
-  cluster_sync();  // (1) per-CTA counts published
+  cluster_sync();  // [S3] stamps visible, per-CTA counts published
   if (tid == 0) {
     uint32_t before = 0;
     sh.n_miss_total = static_cast<int>(sum_over_cluster(&sh.pub_nmiss, rank, &before));
@@ -406,193 +737,161 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     sh.hits_total[tid] = static_cast<int>(sum_over_cluster(&sh.pub_hit[tid], rank, &before));
     sh.hit_off[tid] = static_cast<int>(before);
   }
+  // LRU positions of this CTA in the current order list
+  const int step_b = step0;
+  const int per_wc = (((cl + NW - 1) / NW) + 31) & ~31;
+  const int clo = warp * per_wc;
+  const int chi = clo + per_wc < cl ? clo + per_wc : cl;
+  {
+    // unstamped entries among my positions of the list (hits were stamped)
+    int cnt = 0;
+    for (int i = tid; i < cl; i += NT) {
+      int s = cslot[i];
+      if (s < 0 || s >= a.C) {
+        set_status(a.status, ESS_ERR_DEVICE_CHECK);
+        s = 0;
+      }
+      cslot[i] = s;
+      const bool u = a.last_used[bC + s] != step_b;
+      cflag[i] = u ? 1 : 0;
+      cnt += u ? 1 : 0;
+    }
+    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0 && cnt) atomicAdd(&sh.pub_unst, cnt);
+  }
   __syncthreads();
-  const int n_miss_total = sh.n_miss_total;
+  int n_miss_total = sh.n_miss_total;
   if (n_miss_total > a.C || n_miss_total > MK) {  // cannot happen when C >= min(M*k, T)
     if (tid == 0) set_status(a.status, ESS_ERR_CAPACITY);
+    n_miss_total = 0;
   }
-  // (2) the miss union in ascending token order
   {
+    // the miss union in ascending token order; prefetch each miss row into L2
     int run = sh.miss_off;
     for (int base = 0; base < nu; base += NT) {
       const int e = base + tid;
-      const bool f = e < nu && uslot[e] < 0;
-      int tot;
-      const int pos = run + block_scan(f ? 1 : 0, tot, sh, parity);
-      if (f && pos < MK) a.miss_tok[static_cast<size_t>(b) * MK + pos] = utok[e];
-      run += tot;
+      const bool f = e < nu && lslot[e] < 0;
+      const int pos = ordered_pos(f ? 1 : 0, run, sh, parity);
+      if (f && pos < MK) {
+        const int t = ltok[e];
+        a.miss_tok[static_cast<size_t>(b) * MK + pos] = t;
+        if (a.host != nullptr) {
+          int prow = t;
+          if (a.page_table)
+            prow = a.page_table[static_cast<size_t>(b) * (a.T / a.page) + t / a.page] * a.page +
+                   t % a.page;
+          if (prow >= 0 && prow < a.T)
+            bulk_prefetch_l2(a.host + (bT + prow) * kRowDim, kRowBytes);
+        }
+      }
     }
   }
-  __threadfence();
   __syncthreads();
-  cluster_sync();  // (2) stamps and miss list visible
-
-  // ---------------------------------------------------------------- (a4) LRU victims
-  const bool do_victims = n_miss_total > 0 && n_miss_total <= a.C && n_miss_total <= MK;
-  if (do_victims) {
-    const int s0 = static_cast<int>(rank) * a.c_local;
-    int cl = a.C - s0;
-    cl = cl < 0 ? 0 : (cl > a.c_local ? a.c_local : cl);
-    int mn = 0x7fffffff, mx = -0x7fffffff - 1;
+  cluster_sync();  // [S4] unstamped counts published, miss list visible
+  if (tid == 0) {
+    uint32_t before = 0;
+    sh.unst_total = static_cast<int>(sum_over_cluster(&sh.pub_unst, rank, &before));
+    sh.unst_before = static_cast<int>(before);
+  }
+  __syncthreads();
+  {
+    // unstamped slots in LRU order: the first |Miss| are the victims, the rest
+    // open the next list (each warp places its own contiguous positions)
+    int wcnt = 0;
+    for (int base = clo; base < chi; base += 32) {
+      const int i = base + lane;
+      wcnt += __popc(__ballot_sync(0xffffffffu, i < chi && cflag[i]));
+    }
+    int total;
+    int pos = sh.unst_before + warp_base(wcnt, total, sh);
+    for (int base = clo; base < chi; base += 32) {
+      const int i = base + lane;
+      const bool f = i < chi && cflag[i];
+      const unsigned bal = __ballot_sync(0xffffffffu, f);
+      if (f) {
+        const int p = pos + __popc(bal & lt);
+        if (p < n_miss_total)
+          a.vlist[static_cast<size_t>(b) * MK + p] = cslot[i];
+        else if (p - n_miss_total < a.C)
+          onxt[p - n_miss_total] = cslot[i];
+      }
+      pos += __popc(bal);
+    }
+  }
+  __syncthreads();  // cflag (list flags) is reused below as per-slot stamped flags
+  {
+    // hits among my slot range (victims are not stamped yet)
+    int cnt = 0;
     for (int i = tid; i < cl; i += NT) {
-      const int v = a.last_used[bC + s0 + i];
-      lu_s[i] = v;
-      mn = v < mn ? v : mn;
-      mx = v > mx ? v : mx;
+      const bool h = a.last_used[bC + p0 + i] == step_b;
+      cflag[i] = h ? 1 : 0;
+      cnt += h ? 1 : 0;
     }
-    for (int o = 16; o; o >>= 1) {
-      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    if (tid == 0) {
-      sh.pub_lumin = 0x7fffffff;
-      sh.pub_lumax = -0x7fffffff - 1;
-    }
-    __syncthreads();
-    if ((tid & 31) == 0) {
-      atomicMin(&sh.pub_lumin, mn);
-      atomicMax(&sh.pub_lumax, mx);
-    }
-    __syncthreads();
-    cluster_sync();  // (3)
-    if (tid == 0) {
-      int gmn = 0x7fffffff, gmx = -0x7fffffff - 1;
-      for (uint32_t r = 0; r < CL; ++r) {
-        gmn = min(gmn, static_cast<int>(ld_dsmem_u32(dsmem_addr(smem_u32(&sh.pub_lumin), r))));
-        gmx = max(gmx, static_cast<int>(ld_dsmem_u32(dsmem_addr(smem_u32(&sh.pub_lumax), r))));
-      }
-      sh.lu_min = gmn;
-      sh.lu_max = gmx;
-      sh.active[0] = n_miss_total < a.C ? 1 : 0;
-      for (int m = 1; m < kMaxWays; ++m) sh.active[m] = 0;
-      sh.remaining[0] = n_miss_total;
-    }
-    __syncthreads();
-    const int lu_max = sh.lu_max;
-    const uint32_t range = static_cast<uint32_t>(lu_max - sh.lu_min);
-    const int nbits = range == 0 ? 0 : 32 - __clz(static_cast<int>(range));
-    // larger key = older slot; equal keys go to the lowest slot
-    auto lu_key = [&](int, int i) -> uint32_t { return static_cast<uint32_t>(lu_max - lu_s[i]); };
-    const bool take_all = !sh.active[0];
-    if (!take_all) {
-      if (nbits > 0) {
-        cluster_select(lu_key, cl, 1, nbits, sh, rank);
-      } else {
-        if (tid == 0) {
-          sh.prefix[0] = 0;
-          sh.eq_local[0] = cl;
-          const int bef = s0 < a.C ? s0 : a.C;
-          sh.eq_before[0] = bef;
-          sh.eq_total[0] = a.C;
-        }
-        __syncthreads();
-      }
-      set_quota(sh, 1);
-      __syncthreads();
-    }
-    // victims in slot order: count, exchange, write
-    const uint32_t thr = sh.prefix[0];
-    int vcnt = 0;
-    for (int base = 0; base < cl; base += NT) {
-      const int i = base + tid;
-      int f = 0;
-      if (i < cl) f = take_all ? 1 : (lu_key(0, i) > thr ? 1 : 0);
-      vcnt += f;
-    }
-    for (int o = 16; o; o >>= 1) vcnt += __shfl_xor_sync(0xffffffffu, vcnt, o);
-    if ((tid & 31) == 0) atomicAdd(&sh.pub_vcnt, vcnt);
-    __syncthreads();
-    if (tid == 0 && !take_all) sh.pub_vcnt += sh.quota[0];
-    __syncthreads();
-    cluster_sync();  // (4)
-    if (tid == 0) {
-      uint32_t before = 0;
-      sum_over_cluster(&sh.pub_vcnt, rank, &before);
-      sh.vict_off = static_cast<int>(before);
-    }
-    __syncthreads();
-    {
-      int run = sh.vict_off;
-      int eqr = 0;
-      for (int base = 0; base < cl; base += NT) {
-        const int i = base + tid;
-        bool f = false;
-        if (i < cl) {
-          if (take_all) {
-            f = true;
-          } else {
-            const uint32_t kk = lu_key(0, i);
-            if (kk > thr) f = true;
-          }
-        }
-        bool e = false;
-        if (!take_all && i < cl && lu_key(0, i) == thr) e = true;
-        if (!take_all && sh.rank_needed[0]) {
-          int tot;
-          const int r = eqr + block_scan(e ? 1 : 0, tot, sh, parity);
-          if (e && r < sh.quota[0]) f = true;
-          eqr += tot;
-        } else if (!take_all && e && sh.quota[0] > 0) {
-          f = true;
-        }
-        int tot;
-        const int pos = run + block_scan(f ? 1 : 0, tot, sh, parity);
-        if (f && pos < MK) {
-          const int slot = s0 + i;
-          const uint32_t lub = static_cast<uint32_t>(lu_s[i]) ^ 0x80000000u;
-          a.vict[static_cast<size_t>(b) * MK + pos] =
-              (static_cast<unsigned long long>(lub) << 32) | static_cast<uint32_t>(slot);
-        }
-        run += tot;
+    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0 && cnt) atomicAdd(&sh.pub_stamp, cnt);
+  }
+  __syncthreads();
+  cluster_sync();  // [S5] victims listed
+  {
+    // victims in my slot range complete the stamped slots
+    int cnt = 0;
+    for (int i = tid; i < n_miss_total; i += NT) {
+      const int v = a.vlist[static_cast<size_t>(b) * MK + i];
+      if (v >= p0 && v < p0 + cl) {
+        cflag[v - p0] = 1;
+        ++cnt;
       }
     }
-    __threadfence();
-    __syncthreads();
-    cluster_sync();  // (5) victims gathered
-    if (rank == 0) {
-      // sort the victims by (last_used, slot) and pair them with the misses
-      unsigned long long* sb = reinterpret_cast<unsigned long long*>(keys_s);
-      const int n = n_miss_total;
-      int np2 = 1;
-      while (np2 < n) np2 <<= 1;
-      for (int i = tid; i < np2; i += NT)
-        sb[i] = i < n ? a.vict[static_cast<size_t>(b) * MK + i] : ~0ull;
-      __syncthreads();
-      for (int kk = 2; kk <= np2; kk <<= 1) {
-        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-          for (int i = tid; i < np2; i += NT) {
-            const int ix = i ^ jj;
-            if (ix > i) {
-              const unsigned long long x = sb[i], y = sb[ix];
-              const bool up = (i & kk) == 0;
-              if ((x > y) == up) {
-                sb[i] = y;
-                sb[ix] = x;
-              }
-            }
-          }
-          __syncthreads();
-        }
+    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0 && cnt) atomicAdd(&sh.pub_stamp, cnt);
+  }
+  if (n_miss_total > 0) {
+    // pair the i-th miss with the i-th victim, split across the cluster
+    const int per = (n_miss_total + CL - 1) / CL;
+    const int i0 = static_cast<int>(rank) * per;
+    const int i1 = i0 + per < n_miss_total ? i0 + per : n_miss_total;
+    for (int i = i0 + tid; i < i1; i += NT) {
+      const int v = a.vlist[static_cast<size_t>(b) * MK + i];
+      const int t = a.miss_tok[static_cast<size_t>(b) * MK + i];
+      if (v < 0 || v >= a.C || t < 0 || t >= Tb) {
+        set_status(a.status, ESS_ERR_DEVICE_CHECK);
+        continue;
       }
-      const int step_b = sh.step_b;
-      for (int i = tid; i < n; i += NT) {
-        const int v = static_cast<int>(sb[i] & 0xffffffffu);
-        const int t = a.miss_tok[static_cast<size_t>(b) * MK + i];
-        if (v < 0 || v >= a.C || t < 0 || t >= Tb) {
-          set_status(a.status, ESS_ERR_DEVICE_CHECK);
-          continue;
-        }
-        const int old = a.slot_token[bC + v];
-        if (old >= 0 && old < a.T) a.cache_slots[bT + old] = -1;
-        a.cache_slots[bT + t] = v;
-        a.slot_token[bC + v] = t;
-        a.last_used[bC + v] = step_b;
-        a.miss_slot[static_cast<size_t>(b) * MK + i] = v;
-      }
+      const int old = a.slot_token[bC + v];
+      if (old >= 0 && old < a.T) a.cache_slots[bT + old] = -1;
+      a.cache_slots[bT + t] = v;
+      a.slot_token[bC + v] = t;
+      a.last_used[bC + v] = step_b;
+      a.miss_slot[static_cast<size_t>(b) * MK + i] = v;
     }
-    __threadfence();
-    __syncthreads();
-    cluster_sync();  // (6) new slots visible
+  }
+  __syncthreads();
+  cluster_sync();  // [S6] new slots visible, stamped counts published
+  if (tid == 0) {
+    uint32_t before = 0;
+    sum_over_cluster(&sh.pub_stamp, rank, &before);
+    sh.stamp_before = static_cast<int>(before);
+  }
+  __syncthreads();
+  {
+    // stamped slots (hits and victims) close the next list in slot order
+    int wcnt = 0;
+    for (int base = clo; base < chi; base += 32) {
+      const int i = base + lane;
+      wcnt += __popc(__ballot_sync(0xffffffffu, i < chi && cflag[i]));
+    }
+    int total;
+    int pos = sh.unst_total - n_miss_total + sh.stamp_before + warp_base(wcnt, total, sh);
+    for (int base = clo; base < chi; base += 32) {
+      const int i = base + lane;
+      const bool f = i < chi && cflag[i];
+      const unsigned bal = __ballot_sync(0xffffffffu, f);
+      if (f) {
+        const int p = pos + __popc(bal & lt);
+        if (p < a.C) onxt[p] = p0 + i;
+      }
+      pos += __popc(bal);
+    }
   }
 
   // ---------------------------------------------------------------- emit per-way lists
@@ -604,15 +903,14 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       const int e = base + tid;
       bool fm = false, fh = false;
       int t = 0, s = -1;
-      if (e < nu && (umask[e] & (1u << m))) {
-        t = utok[e];
-        s = uslot[e];
+      if (e < nu && (lflag[e] & (1u << m))) {
+        t = ltok[e];
+        s = lslot[e];
         fm = s < 0;
         fh = !fm;
       }
-      int totm, toth;
-      const int pm = runm + block_scan(fm ? 1 : 0, totm, sh, parity);
-      const int ph = runh + block_scan(fh ? 1 : 0, toth, sh, parity);
+      const int pm = ordered_pos(fm ? 1 : 0, runm, sh, parity);
+      const int ph = ordered_pos(fh ? 1 : 0, runh, sh, parity);
       if (fm && pm < a.k) {
         const int ns = a.cache_slots[bT + t];
         a.topk_idx[wo + pm] = t;
@@ -622,14 +920,12 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         a.topk_idx[wo + ph] = t;
         a.topk_slot[wo + ph] = s;
       }
-      runm += totm;
-      runh += toth;
     }
   }
   if (rank == 0 && tid == 0) {
     for (int m = 0; m < M; ++m) a.n_miss_way[b * M + m] = sh.nmw[m];
     a.n_miss[b] = n_miss_total;
-    a.step[b] = sh.step_b + 1;
+    a.step[b] = step_b + 1;
     if (a.stats) {
       long long h = 0, mi = 0;
       for (int m = 0; m < M; ++m) {
@@ -649,21 +945,39 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   }
   __syncthreads();
   cluster_sync();  // nobody leaves while others may read its shared memory
+  // every CTA has read the histogram: clear it for the next step
+  if (rank == 0)
+    for (int i = tid; i < M * kHistBins; i += NT) gh[i] = 0u;
+}
+
+__global__ void order_reset_kernel(int32_t* order, int n_per_list, int C) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < 2 * n_per_list) order[i] = (i % n_per_list) % C;
 }
 
 }  // namespace
 
-cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, int32_t* topk_idx,
-                          int32_t* topk_slot, int32_t* n_miss_way, int32_t* miss_tok,
-                          int32_t* miss_slot, int32_t* n_miss, cudaStream_t st) {
+cudaError_t launch_order_reset(const ess_pool& p, int layer, cudaStream_t st) {
+  const ess_config& c = p.cfg;
+  const int n = c.batch * c.C;
+  order_reset_kernel<<<(2 * n + 255) / 256, 256, 0, st>>>(p.layers[layer].order, n, c.C);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, bool hist_given,
+                          int32_t* topk_idx, int32_t* topk_slot, int32_t* n_miss_way,
+                          int32_t* miss_tok, int32_t* miss_slot, int32_t* n_miss, cudaStream_t st) {
   const ess_config& c = p.cfg;
   const Layer& L = p.layers[layer];
   SelArgs a;
   a.scores = scores;
+  a.ghist = p.scr.ghist;
+  a.hist_given = hist_given ? 1 : 0;
   a.cache_slots = L.cache_slots;
   a.slot_token = L.slot_token;
   a.last_used = L.last_used;
   a.step = L.step;
+  a.order = L.order;
   a.Tb = L.T_dev;
   a.topk_idx = topk_idx;
   a.topk_slot = topk_slot;
@@ -671,7 +985,10 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, int
   a.miss_tok = miss_tok;
   a.miss_slot = miss_slot;
   a.n_miss = n_miss;
-  a.vict = p.scr.vict;
+  a.vlist = p.scr.vlist;
+  a.host = L.host_latent;
+  a.page_table = L.page_table;
+  a.page = c.page;
   a.stats = L.stats;
   a.status = p.scr.status;
   a.B = c.batch;
@@ -685,15 +1002,15 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, int
   a.n_local = nl;
   a.c_local = (c.C + CL - 1) / CL;
   const int MK = c.mtp * c.k;
-  a.ucap = MK < c.mtp * nl ? MK : c.mtp * nl;
-  int np2 = 1;
-  while (np2 < MK) np2 <<= 1;
-  const size_t sort_bytes = static_cast<size_t>(np2) * 8;
+  a.lcap = nl < MK ? nl : MK;   // the union of one CTA's tokens never exceeds this
+  a.lcap = (a.lcap + 3) / 4 * 4; // keeps the arrays after the list 16-byte aligned
+  a.gcap = 4096;
   const size_t res_bytes = static_cast<size_t>(c.mtp) * nl * 4;
-  const size_t fixed = static_cast<size_t>(a.c_local) * 4 + static_cast<size_t>(a.ucap) * 9 + 64;
-  const size_t budget = 200 * 1024;
+  const size_t fixed = static_cast<size_t>(a.lcap) * (9 + 4 * c.mtp) +
+                       static_cast<size_t>(a.c_local) * 5 + static_cast<size_t>(a.gcap) * 5 + 64;
+  const size_t budget = 160 * 1024;   // leaves room for the static shared state
   a.resident = (res_bytes + fixed <= budget) ? 1 : 0;
-  size_t kb = a.resident ? (res_bytes > sort_bytes ? res_bytes : sort_bytes) : sort_bytes;
+  size_t kb = a.resident ? res_bytes : 0;
   kb = (kb + 15) / 16 * 16;
   a.keys_bytes = static_cast<uint32_t>(kb);
   const size_t smem = kb + fixed;

@@ -30,9 +30,11 @@ ESS_MISS_STAGED = 1
 
 # every exported symbol of include/ess.h
 EXPORTS = (
-    "ess_status_string", "ess_pool_device_bytes", "ess_pool_create", "ess_pool_destroy",
+    "ess_status_string", "ess_host_alloc", "ess_host_free", "ess_pool_device_bytes",
+    "ess_pool_create", "ess_pool_destroy",
     "ess_pool_bind_layer", "ess_pool_reset", "ess_indexer_scores", "ess_select_manage",
-    "ess_indexer_topk", "ess_stage_misses", "ess_sparse_mla_decode", "ess_step", "ess_step_host",
+    "ess_indexer_topk", "ess_stage_misses", "ess_sparse_mla_decode", "ess_step",
+    "ess_step_profiled", "ess_step_host",
     "ess_pipeline_step", "ess_pool_get_state", "ess_pool_set_state", "ess_pool_get_rows",
     "ess_pool_read_stats", "ess_pool_poll",
 )
@@ -77,6 +79,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ess_status_string.restype = ctypes.c_char_p
     lib.ess_status_string.argtypes = [I]
     sigs = {
+        "ess_host_alloc": [ctypes.c_size_t, ctypes.POINTER(P)],
+        "ess_host_free": [P],
         "ess_pool_device_bytes": [ctypes.POINTER(ess_config), ctypes.POINTER(ctypes.c_size_t)],
         "ess_pool_create": [ctypes.POINTER(ess_config), P, ctypes.c_size_t, ctypes.POINTER(P)],
         "ess_pool_destroy": [P],
@@ -88,6 +92,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "ess_stage_misses": [P, I, P, P, P, P],
         "ess_sparse_mla_decode": [P, I, P, P, P, P, P],
         "ess_step": [P, I, P, P, P, P, P],
+        "ess_step_profiled": [P, I, P, P, P, P, P, P],
         "ess_step_host": [P, I, P, P, P, P, P],
         "ess_pipeline_step": [P, I, I, P, P, P, P, P],
         "ess_pool_get_state": [P, I, P, P, P, P],
@@ -130,6 +135,38 @@ def _stream(stream) -> Optional[int]:
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+class HostBuffer:
+    """Host memory from ess_host_alloc (huge-page backed, registered with CUDA),
+    exposed as a numpy array; freed with close()."""
+
+    def __init__(self, shape, dtype):
+        import numpy as np
+        self.dtype = np.dtype(dtype)
+        self.shape = tuple(int(x) for x in shape)
+        n = int(np.prod(self.shape)) * self.dtype.itemsize
+        p = ctypes.c_void_p(0)
+        check(load().ess_host_alloc(max(n, 1), ctypes.byref(p)), "ess_host_alloc")
+        self.ptr = p.value
+        self.nbytes = n
+        buf = (ctypes.c_char * max(n, 1)).from_address(self.ptr)
+        self.array = np.frombuffer(buf, dtype=self.dtype, count=n // self.dtype.itemsize).reshape(self.shape)
+
+    def data_ptr(self):
+        return self.ptr
+
+    def close(self):
+        if self.ptr:
+            self.array = None
+            check(load().ess_host_free(self.ptr), "ess_host_free")
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def make_config(*, n_layers, batch, max_T, C, k, mtp, idx_heads, idx_dim, idx_dtype, mla_heads,
@@ -197,6 +234,14 @@ def ess_sparse_mla_decode(pool, layer, q_mla, topk_idx, topk_slot, out, stream=N
 def ess_step(pool, layer, q_idx, w, q_mla, out, stream=None) -> None:
     check(load().ess_step(pool, layer, _p(q_idx), _p(w), _p(q_mla), _p(out), _stream(stream)),
           "ess_step")
+
+
+def ess_step_profiled(pool, layer, q_idx, w, q_mla, out, events, stream=None) -> None:
+    """events: four torch.cuda.Event (or None) recorded between the phases."""
+    hs = [None if e is None else e.cuda_event for e in events]
+    arr = (ctypes.c_void_p * 4)(*hs)
+    check(load().ess_step_profiled(pool, layer, _p(q_idx), _p(w), _p(q_mla), _p(out),
+                                   _stream(stream), arr), "ess_step_profiled")
 
 
 def ess_step_host(pool, layer, q_idx, w, q_mla, out, stream=None) -> None:

@@ -28,7 +28,9 @@ def ess_config_of(cfg: W.WorkloadConfig, miss_mode: int = ess.ESS_MISS_FUSED,
 class Session:
     def __init__(self, cfg: W.WorkloadConfig, layers: List[W.LayerData],
                  miss_mode: int = ess.ESS_MISS_FUSED, device: str = "cuda",
-                 keep_host_numpy: bool = False):
+                 host_buffers: Optional[List["ess.HostBuffer"]] = None):
+        """host_buffers: latent caches already in host memory (one per layer),
+        shared with another session; by default each layer gets its own."""
         ess.load()
         self.cfg = cfg
         self.device = torch.device(device)
@@ -39,12 +41,17 @@ class Session:
         self.ws_view = self.workspace[off:off + nbytes]
         self.pool = ess.ess_pool_create(self.ecfg, self.ws_view)
         self.keys, self.scale, self.pages, self.host, self.T = [], [], [], [], []
+        self._own_host = []
         for l, ld in enumerate(layers):
             keys = torch.from_numpy(ld.idx_keys).to(self.device)
             scale = torch.from_numpy(ld.idx_scale).to(self.device)
             pages = torch.from_numpy(ld.page_table).to(self.device)
-            host = torch.empty(ld.host_latent.shape, dtype=torch.int16, pin_memory=True)
-            host.numpy()[...] = ld.host_latent.view(np.int16)
+            if host_buffers is not None:
+                host = host_buffers[l]
+            else:
+                host = ess.HostBuffer(ld.host_latent.shape, np.uint16)
+                host.array[...] = ld.host_latent
+                self._own_host.append(host)
             T = torch.from_numpy(ld.T.astype(np.int32))
             ess.ess_pool_bind_layer(self.pool, l, host, pages, keys, scale, T)
             self.keys.append(keys)
@@ -122,6 +129,9 @@ class Session:
         if self.pool:
             ess.ess_pool_destroy(self.pool)
             self.pool = None
+        for h in self._own_host:
+            h.close()
+        self._own_host = []
 
     def __del__(self):
         try:

@@ -126,6 +126,17 @@ ess_status ess_pool_create(const ess_config* cfg, void* dev_workspace, size_t ws
 /* Release the handle (the caller frees the workspace). */
 ess_status ess_pool_destroy(ess_pool* pool);
 
+/* Allocate host memory for a latent cache: an anonymous mapping aligned to
+ * the transparent-huge-page size and advised for huge pages (fewer GPU
+ * translations of host pages when misses read scattered rows), touched, and
+ * registered with CUDA so that kernels can read it (pinned, mapped).  The
+ * memory is zero-filled.  Release it with ess_host_free.  Errors:
+ * ESS_ERR_OOM (mapping failed), ESS_ERR_CUDA (registration failed). */
+ess_status ess_host_alloc(size_t bytes, void** out);
+
+/* Unregister and unmap memory from ess_host_alloc. */
+ess_status ess_host_free(void* ptr);
+
 /* Bind the inputs of one layer ([FO] "architecture": host master copy
  * behind a block table; [ESS]: indexer cache resident on the GPU).
  *   host_latent  pinned host, [B][T][D] bf16, physical rows: logical token t
@@ -145,8 +156,9 @@ ess_status ess_pool_reset(ess_pool* pool, int layer, ess_stream_t stream);
 
 /* (a1) Indexer scores ([ESS]: score all positions; formula
  * S[b][m][t] = fl32(scale[b][t] * sum_h w[b][m][h] * ReLU(q[b][m][h] . k[b][t]))).
- *   q_idx   device [B][M][H_I][128 bytes] (same encoding as the keys)
- *   w       device float [B][M][H_I]
+ *   q_idx   device [B][M][H_I][128 bytes] (same encoding as the keys),
+ *           16-byte aligned
+ *   w       device float [B][M][H_I], 16-byte aligned (M * H_I a multiple of 4)
  *   scores  device float [B][M][T]; entries t >= T_b are not written */
 ess_status ess_indexer_scores(ess_pool* pool, int layer, const void* q_idx, const float* w,
                               float* scores, ess_stream_t stream);
@@ -206,6 +218,14 @@ ess_status ess_sparse_mla_decode(ess_pool* pool, int layer, const void* q_mla,
  *   ess_sparse_mla_decode. */
 ess_status ess_step(ess_pool* pool, int layer, const void* q_idx, const float* w,
                     const void* q_mla, float* out, ess_stream_t stream);
+
+/* ess_step with measurement hooks: the same launches as ess_step, and
+ * events[i] (each a cudaEvent_t, or NULL to skip) is recorded on stream
+ * before the indexer (0), after the indexer (1), after selection and
+ * staging (2) and after attention (3). */
+ess_status ess_step_profiled(ess_pool* pool, int layer, const void* q_idx, const float* w,
+                             const void* q_mla, float* out, ess_stream_t stream,
+                             void* const* events);
 
 /* ess_step with HOST inputs and output: the inputs are copied to device
  * staging, the step runs, and out is copied back, all on stream (pass pinned

@@ -73,7 +73,19 @@ def test_indexer_scores_precision_stress():
 
 # ------------------------------------------------------------------ selection + LRU (a2-a4)
 
-def _select_case(T_list, k, C, M, steps, seed, levels=3, H=16):
+def _planted_ties(rng, shape, k):
+    """Mostly distinct scores with a run of exact ties planted at the k-th largest."""
+    sc = np.exp(rng.normal(0.0, 3.0, size=shape)).astype(np.float32)  # spread over binades
+    B_, M_, T_ = shape
+    for b in range(B_):
+        for m in range(M_):
+            kth = np.sort(sc[b, m])[::-1][min(k, T_) - 1]
+            pos = rng.choice(T_, size=min(60, T_), replace=False)
+            sc[b, m, pos] = kth
+    return sc
+
+
+def _select_case(T_list, k, C, M, steps, seed, levels=3, H=16, planted=False):
     cfg = W.multilayer().replace(layers=1, batch=len(T_list), T=max(max(T_list), 64),
                                  T_per_req=T_list, k=k, C=C, mtp=M, mla_heads=H)
     ld = W.gen_layer(cfg)
@@ -82,8 +94,11 @@ def _select_case(T_list, k, C, M, steps, seed, levels=3, H=16):
     rng = np.random.default_rng(seed)
     Tm = W.t_max_of(cfg)
     for s in range(steps):
-        sc = rng.integers(0, levels, size=(cfg.batch, M, Tm)).astype(np.float32)
-        sc[:, :, ::7] = rng.random((cfg.batch, M, len(range(0, Tm, 7)))).astype(np.float32)
+        if planted:
+            sc = _planted_ties(rng, (cfg.batch, M, Tm), k)
+        else:
+            sc = rng.integers(0, levels, size=(cfg.batch, M, Tm)).astype(np.float32)
+            sc[:, :, ::7] = rng.random((cfg.batch, M, len(range(0, Tm, 7)))).astype(np.float32)
         st = torch.from_numpy(sc).cuda()
         sess.select(0, st)
         torch.cuda.synchronize()
@@ -133,6 +148,16 @@ def test_select_k_at_least_T_and_empty_request():
 
 def test_select_all_equal_scores():
     _select_case([5000, 4096], k=256, C=512, M=1, steps=5, seed=3, levels=1)
+
+
+def test_select_threshold_ties_candidate_path():
+    # few candidates per histogram bin: the candidate-refinement path, with
+    # exact ties at the k-th score spread over every CTA's token range
+    _select_case([20000, 9000], k=512, C=1200, M=2, steps=5, seed=5, planted=True)
+
+
+def test_select_threshold_ties_one_way_large_T():
+    _select_case([131072], k=2048, C=4096, M=1, steps=3, seed=6, planted=True)
 
 
 def test_select_many_ties_small_pool():
@@ -250,3 +275,41 @@ def test_two_microbatch_layer_pipeline():
                 assert_attn_close(out.cpu().numpy(), r.out, f"pipeline h={h} l={l}")
     for p in pairs:
         p.close()
+
+
+# ------------------------------------------------------------------ state set/get (resume)
+
+def test_set_state_resumes_from_oracle_state():
+    """A fresh pool given the oracle's state after some steps continues in step
+    with the oracle (lists and bookkeeping; the LRU order is rebuilt)."""
+    cfg = W.tiny().replace(T=2048, k=128, C=256)
+    p = Pair(cfg)
+    for _ in range(3):
+        p.run_step()
+    q = Pair(cfg)
+    for _ in range(3):   # advance the second pair's query stream and oracle only
+        q.next_inputs(0)
+    for b in range(cfg.batch):
+        q.orc[0].state[b] = p.orc[0].state[b].copy()
+    st = p.orc[0].state[0]
+    Tm = W.t_max_of(cfg)
+    cs = np.full((1, Tm), -1, np.int32)
+    cs[0, :len(st.cache_slots)] = st.cache_slots
+    ess.ess_pool_set_state(q.sess.pool, 0, torch.from_numpy(cs), torch.from_numpy(st.slot_token[None].copy()),
+                           torch.from_numpy(st.last_used[None].copy()),
+                           torch.tensor([st.step], dtype=torch.int32))
+    q.compare_state(0)
+    for _ in range(3):
+        q.run_step(check_out=False)
+    p.close()
+    q.close()
+
+
+def test_set_state_rejects_future_stamps():
+    cfg = W.tiny().replace(T=1024, k=64, C=128)
+    p = Pair(cfg)
+    lu = torch.full((1, cfg.C), -1, dtype=torch.int32)
+    lu[0, 5] = 7
+    with pytest.raises(ess.EssError):
+        ess.ess_pool_set_state(p.sess.pool, 0, None, None, lu, torch.tensor([3], dtype=torch.int32))
+    p.close()
