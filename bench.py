@@ -62,6 +62,28 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def rank_workload(cfg: W.WorkloadConfig, rank: int) -> W.WorkloadConfig:
+    """Each rank serves its own independent requests (same shapes, its own
+    seed): the decode path shards over requests with no exchange, so the job
+    scales weakly and needs no collective on the data path."""
+    return cfg.replace(seed=cfg.seed + 7919 * rank)
+
+
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings (a barrier-bracketed job is as
+    slow as its slowest rank)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_throughput(units_per_step_per_rank: int, world: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job units per second: every rank's units over the slowest rank's time."""
+    return world * units_per_step_per_rank * steps / (elapsed_ms / 1e3)
+
+
 def config_json(cfg: W.WorkloadConfig, n_gpus: int, miss_mode: str):
     return {
         "workload": f"{cfg.name}: batch {cfg.batch} x T={cfg.T}, top-k {cfg.k}, "
@@ -239,15 +261,15 @@ def measure_overlap(cfg, ld, n_steps, stream, host_buffers):
     and T_fused (attention that reads misses from host memory itself), per
     step, and OverlapRatio = (T_copy + T_SFA - T_fused) / T_copy.  A fused pool
     runs the steps first, then a staged pool replays the same inputs from the
-    same empty state (identical selections and misses), one pool at a time."""
+    same empty state (identical selections and misses), one pool at a time;
+    both read the latent cache of the main session's host buffer."""
     import torch
     from host_latent_cache_gb300 import ess
     from host_latent_cache_gb300.session import Session
     qs = W.QueryStream(cfg)
     wts = W.head_weights(cfg, ld.w)
     steps = [qs.next() for _ in range(n_steps)]
-    res = {}
-    outs = {}
+    res, outs = {}, {}
     for mode in (ess.ESS_MISS_FUSED, ess.ESS_MISS_STAGED):
         sess = Session(cfg, [ld], miss_mode=mode, host_buffers=host_buffers)
         rows = []
@@ -302,7 +324,7 @@ def bench_ours(args, cfg, rank, world, local_rank):
         dist.barrier()
     ess.load()
     # each rank serves its own independent requests (weak scaling)
-    cfg_r = cfg.replace(seed=cfg.seed + 7919 * rank)
+    cfg_r = rank_workload(cfg, rank)
     ld = W.gen_layer(cfg_r)
     mode = ess.ESS_MISS_STAGED if args.miss_mode == "staged" else ess.ESS_MISS_FUSED
     sess = Session(cfg_r, [ld], miss_mode=mode)
@@ -384,13 +406,10 @@ def bench_ours(args, cfg, rank, world, local_rank):
     assert sess.poll(stream) == ess.ESS_OK
     e2e_ms = e_start.elapsed_time(e_end)
 
-    t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], dist, device="cuda")
     units_step = cfg.batch * cfg.mtp * cfg.layers
-    value = world * units_step * nsteps / (elapsed_ms / 1e3)
-    e2e_value = world * units_step * nsteps / (e2e_ms / 1e3)
+    value = job_throughput(units_step, world, nsteps, elapsed_ms)
+    e2e_value = job_throughput(units_step, world, nsteps, e2e_ms)
 
     result = None
     if rank == 0:
