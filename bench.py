@@ -307,6 +307,41 @@ def measure_overlap(cfg, ld, n_steps, stream, host_buffers):
                                                   outs[ess.ESS_MISS_STAGED]))}
 
 
+# sources of the indexer kernel; the DRAM traffic taken by ncu holds only
+# while they are unchanged
+INDEXER_SOURCES = ("ess_indexer.cu", "ess_device.cuh", "ess_internal.h")
+
+
+def indexer_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in INDEXER_SOURCES:
+        with open(os.path.join(ROOT, "host_latent_cache_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def indexer_traffic(cfg):
+    """DRAM bytes (read + write) per indexer launch from the committed ncu
+    summary of this workload, or None when there is none or the kernel's
+    sources have changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"indexer_{cfg.name}.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and not line.lstrip().startswith("#"):
+                k, v = line.split("=", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("source_digest") != indexer_source_digest():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def bench_ours(args, cfg, rank, world, local_rank):
     import torch
     from host_latent_cache_gb300 import build as B
@@ -430,13 +465,7 @@ def bench_ours(args, cfg, rank, world, local_rank):
         r_idx_us = idx_bytes / (hbm_peak * 1e9) * 1e6
         r_hit_us = hit_rows * ROW_BYTES / (hbm_peak * 1e9) * 1e6
         step_us = elapsed_ms * 1e3 / nsteps
-        traffic = None
-        tr_path = os.path.join(ROOT, "profiles", "indexer_traffic.json")
-        if os.path.exists(tr_path):
-            try:
-                traffic = json.load(open(tr_path)).get("dram_bytes_per_launch")
-            except Exception:
-                traffic = None
+        traffic = indexer_traffic(cfg)
         result = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": nsteps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / nsteps, "higher_is_better": True,
