@@ -37,6 +37,8 @@
 // |Miss| of them are the victims, already in the order that pairs the i-th
 // miss with the i-th victim; the next list is the remaining unstamped
 // entries followed by the stamped slots in slot order.
+#include <mutex>
+
 #include "ess_device.cuh"
 
 namespace ess {
@@ -1021,4 +1023,75 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Selection whose scratch needs no allocation by the caller.
+//
+// For callers that cannot allocate device memory when they select: an engine
+// that hands out all of its device memory at start-up, or a thread on which an
+// allocation would synchronise the device and stall decoding.  The selection
+// kernel needs two scratch buffers besides its inputs, outputs and the pool
+// state: the per-(request, way) score histogram and the victim list.  This
+// variant takes them from a fixed array compiled into the library instead of
+// the pool's workspace.  Every GPU that loads the library holds the array
+// until the process exits; every call shares it, so calls that overlap on the
+// GPU race.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kSelectStaticScratchBytes = size_t(2) << 20;  // 2 MiB
+
+static __device__ __align__(256) unsigned char g_select_scratch[kSelectStaticScratchBytes];
+
+// Device address of g_select_scratch, looked up once per device (the name is
+// only a host-side stand-in for the device array).
+std::mutex g_scratch_mu;
+void* g_scratch_addr[128] = {nullptr};
+
+cudaError_t select_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> g(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_select_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+size_t align256_sz(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
 }  // namespace ess
+
+extern "C" ess_status ess_select_manage_noalloc(ess_pool* pool, int layer, const float* scores,
+                                                int32_t* topk_idx, int32_t* topk_slot,
+                                                int32_t* n_miss_way, int32_t* miss_tok,
+                                                int32_t* miss_slot, int32_t* n_miss,
+                                                ess_stream_t stream) {
+  using namespace ess;
+  if (!pool || layer < 0 || layer >= pool->cfg.n_layers || !pool->layers[layer].bound ||
+      !scores || !topk_idx || !topk_slot || !n_miss_way || !miss_tok || !miss_slot || !n_miss ||
+      (reinterpret_cast<uintptr_t>(scores) & 15u))
+    return ESS_ERR_INVALID_ARG;
+  const ess_config& c = pool->cfg;
+  const size_t bm = static_cast<size_t>(c.batch) * c.mtp;
+  const size_t hist_bytes = align256_sz(bm * kHistBins * sizeof(uint32_t));
+  const size_t vlist_bytes = align256_sz(bm * c.k * sizeof(int32_t));
+  if (hist_bytes + vlist_bytes > kSelectStaticScratchBytes) return ESS_ERR_OOM;
+  void* base = nullptr;
+  if (select_scratch_address(&base) != cudaSuccess) return ESS_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the histogram is accumulated with atomics, so it must start at zero
+  if (cudaMemsetAsync(base, 0, hist_bytes, st) != cudaSuccess) return ESS_ERR_CUDA;
+  ess_pool view = *pool;  // same layers and state; only the two scratch buffers differ
+  view.scr.ghist = static_cast<uint32_t*>(base);
+  view.scr.vlist = reinterpret_cast<int32_t*>(static_cast<char*>(base) + hist_bytes);
+  const cudaError_t e = launch_select(view, layer, scores, false, topk_idx, topk_slot, n_miss_way,
+                                      miss_tok, miss_slot, n_miss, st);
+  return e == cudaSuccess ? ESS_OK : ESS_ERR_CUDA;
+}

@@ -33,6 +33,7 @@ EXPORTS = (
     "ess_status_string", "ess_host_alloc", "ess_host_free", "ess_pool_device_bytes",
     "ess_pool_create", "ess_pool_destroy",
     "ess_pool_bind_layer", "ess_pool_reset", "ess_indexer_scores", "ess_select_manage",
+    "ess_select_manage_noalloc",
     "ess_indexer_topk", "ess_stage_misses", "ess_sparse_mla_decode", "ess_step",
     "ess_step_profiled", "ess_step_host",
     "ess_pipeline_step", "ess_pool_get_state", "ess_pool_set_state", "ess_pool_get_rows",
@@ -88,6 +89,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "ess_pool_reset": [P, I, P],
         "ess_indexer_scores": [P, I, P, P, P, P],
         "ess_select_manage": [P, I, P, P, P, P, P, P, P, P],
+        "ess_select_manage_noalloc": [P, I, P, P, P, P, P, P, P, P],
         "ess_indexer_topk": [P, I, P, P, P, P, P, P, P, P, P],
         "ess_stage_misses": [P, I, P, P, P, P],
         "ess_sparse_mla_decode": [P, I, P, P, P, P, P],
@@ -212,6 +214,16 @@ def ess_select_manage(pool, layer, scores, topk_idx, topk_slot, n_miss_way, miss
     check(load().ess_select_manage(pool, layer, _p(scores), _p(topk_idx), _p(topk_slot),
                                    _p(n_miss_way), _p(miss_tok), _p(miss_slot), _p(n_miss),
                                    _stream(stream)), "ess_select_manage")
+
+
+def ess_select_manage_noalloc(pool, layer, scores, topk_idx, topk_slot, n_miss_way, miss_tok,
+                              miss_slot, n_miss, stream=None) -> None:
+    """ess_select_manage with its scratch in the library's fixed device array
+    (for callers that cannot provide device scratch)."""
+    check(load().ess_select_manage_noalloc(pool, layer, _p(scores), _p(topk_idx), _p(topk_slot),
+                                           _p(n_miss_way), _p(miss_tok), _p(miss_slot),
+                                           _p(n_miss), _stream(stream)),
+          "ess_select_manage_noalloc")
 
 
 def ess_indexer_topk(pool, layer, q_idx, w, topk_idx, topk_slot, n_miss_way, miss_tok, miss_slot,

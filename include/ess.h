@@ -183,6 +183,28 @@ ess_status ess_select_manage(ess_pool* pool, int layer, const float* scores,
                              int32_t* miss_tok, int32_t* miss_slot, int32_t* n_miss,
                              ess_stream_t stream);
 
+/* ess_select_manage for callers that cannot allocate device memory when they
+ * call it: a serving engine that hands out all of its device memory at
+ * start-up and has none left to give, or code on a thread where an allocation
+ * would synchronise the device and stall decoding.  The pages have no
+ * counterpart; this is a property of this library.
+ * Same arguments, results and state updates as ess_select_manage, but the
+ * selection's scratch (score histogram and victim list, about
+ * B*M*(16 KiB + 4*k) bytes) lives in a fixed 2 MiB array compiled into the
+ * library, which every GPU that loads the library keeps until the process
+ * exits.  It calls no allocator.
+ *   - Returns ESS_ERR_OOM, launching nothing, when the scratch needed exceeds
+ *     the 2 MiB array.
+ *   - The first call on a device looks up the array's device address; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (different
+ *     streams, or several pools at once) race and must be ordered by the
+ *     caller.  The histogram part is cleared at the start of every call. */
+ess_status ess_select_manage_noalloc(ess_pool* pool, int layer, const float* scores,
+                                     int32_t* topk_idx, int32_t* topk_slot, int32_t* n_miss_way,
+                                     int32_t* miss_tok, int32_t* miss_slot, int32_t* n_miss,
+                                     ess_stream_t stream);
+
 /* (a1)-(a4) ess_indexer_scores followed by ess_select_manage, with the
  * scores kept in the pool's scratch ([FO] LIM: LI plus management).
  * Output arguments as in ess_select_manage. */
