@@ -240,6 +240,7 @@ ess_status ess_pool_create(const ess_config* cfg, void* dev_workspace, size_t ws
   ess_pool* p = new (std::nothrow) ess_pool;
   if (!p) return ESS_ERR_OOM;
   p->cfg = *cfg;
+  p->n_launch = &p->launches;
   p->ws = static_cast<char*>(dev_workspace);
   p->ws_bytes = ws_bytes;
   p->device = dev;
@@ -542,6 +543,12 @@ ess_status ess_pool_get_rows(ess_pool* pool, int layer, void* rows_host) {
   if (cudaDeviceSynchronize() != cudaSuccess) return ESS_ERR_CUDA;
   const size_t n = static_cast<size_t>(c.batch) * c.C * kRowBytes;
   return cuda_status(cudaMemcpy(rows_host, pool->layers[layer].pool, n, cudaMemcpyDeviceToHost));
+}
+
+ess_status ess_pool_kernel_launches(const ess_pool* pool, int64_t* count) {
+  if (!pool || !count) return ESS_ERR_INVALID_ARG;
+  *count = pool->launches;
+  return ESS_OK;
 }
 
 ess_status ess_pool_read_stats(ess_pool* pool, int layer, ess_stats* out, int reset) {

@@ -20,11 +20,11 @@
 // significant bits, so the output stays within the tolerance), and
 // O[128][512] = P_hi * V + P_lo * V accumulates in TMEM with V read in place
 // as the N-major operand.
-// Per-CTA (max, sum, O) partials are merged across the chunks of a (request,
-// way): when the chunk CTAs form one thread-block cluster, CTA r reads the
-// others' (max, sum) through distributed shared memory and reduces output
-// dims [r*512/nch, (r+1)*512/nch) from the partials in L2; otherwise a second
-// kernel merges them.
+// Each CTA leaves its (max, sum) per head and its unnormalised O [H][512] as
+// a partial: O leaves TMEM through shared memory in four 128-dim quarters,
+// each written out by one bulk copy.  A second kernel, launched as a
+// programmatic dependent of this one, merges the partials of every (request,
+// way) with the usual log-sum-exp weights.
 #include "ess_device.cuh"
 
 namespace ess {
@@ -50,8 +50,6 @@ struct AttnArgs {
   int B, M, H, k, nch, C, T, page, npages;
   float c2;                   // sm_scale * log2(e)
   int staged;
-  int fused_combine;          // 1: the nch chunk CTAs are one cluster and merge in place
-  float* out;                 // [B][M][H][512] (fused combine)
 };
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -69,7 +67,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* ofull = sfull + 1;                // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ofull + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  __shared__ float2 ml_s[kAttnRows];          // this CTA's (max, sum) per head
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -244,7 +241,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float p[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        p[i] = (cc * 32 + i < cnt) ? exp2f(fmaf(v[i], a.c2, -base)) : 0.0f;
+        p[i] = (cc * 32 + i < cnt) ? ex2_approx(fmaf(v[i], a.c2, -base)) : 0.0f;
         l += p[i];
       }
 #pragma unroll
@@ -294,118 +291,110 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const bool all_o = __syncthreads_and(o_ok ? 1 : 0) != 0;
   const size_t pr = (static_cast<size_t>(b) * a.M + m) * a.nch + c;
   if (all_o) {
-    // partial O stored heads-fastest ([dim][head]) so a warp's stores coalesce
+    // O leaves TMEM through shared memory (the row blocks are free once PV is
+    // done), one 128-dim quarter at a time in two alternating 64 KB buffers:
+    // partial layout [quarter][head][128 dims], the float4 index j of a head's
+    // quarter stored at j ^ (head & 7) so the shared-memory writes spread over
+    // every bank
     tc_fence_after();
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float* dst = a.part_o + pr * kLatent * a.H + tid;
-    for (int cc = 0; cc < kLatent / 32; ++cc) {
-      float v[32];
-      tmem_ld32(trow + cc * 32, v);
-      if (tid < a.H) {
+    float* po = a.part_o + pr * a.H * kLatent;
+    const uint32_t qbytes = static_cast<uint32_t>(a.H) * 128u * 4u;
+    for (int q = 0; q < 4; ++q) {
+      uint8_t* buf = rows + (q & 1) * 65536;
+      if (q >= 2) {
+        if (tid == 0) bulk_wait_read<1>();   // the copy issued from buf two quarters ago
+        __syncthreads();
+      }
+      if (warp * 32 < a.H) {   // tcgen05.ld is warp-wide: the condition is per warp
+        for (int cc = 0; cc < 4; ++cc) {
+          float v[32];
+          tmem_ld32(trow + q * 128 + cc * 32, v);
+          if (tid < a.H) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dst[static_cast<size_t>(cc * 32 + i) * a.H] = v[i];
+            for (int e = 0; e < 8; ++e) {
+              const int jj = cc * 8 + e;
+              *reinterpret_cast<float4*>(buf + tid * 512 + ((jj ^ (tid & 7)) << 4)) =
+                  make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        bulk_store(po + static_cast<size_t>(q) * a.H * 128, smem_u32(buf), qbytes);
+        bulk_commit();
       }
     }
     if (tid < a.H) a.part_ml[pr * a.H + tid] = make_float2(mx, l);
-    ml_s[tid] = make_float2(mx, l);
   } else {
     if (tid < a.H) a.part_ml[pr * a.H + tid] = make_float2(-INFINITY, 0.0f);
-    ml_s[tid] = make_float2(-INFINITY, 0.0f);
   }
+  if (tid == 0) bulk_wait_all();
+  pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (a.fused_combine) {
-    // merge the chunk partials of this (request, way) inside the cluster
-    const int nch = a.nch;
-    const int dpc = kLatent / nch;     // output dims reduced by this CTA
-    const int d0 = c * dpc;
-    cluster_sync();                    // partials (global) and ml_s of every chunk visible
-    float wgt[16];
-    float M = -INFINITY, L = 0.0f;
-    const uint32_t mla = smem_u32(&ml_s[tid]);
-#pragma unroll
-    for (int q = 0; q < 16; ++q) wgt[q] = 0.0f;
-    float2 mlv[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q)
-      mlv[q] = q < nch ? ld_dsmem_f2(dsmem_addr(mla, static_cast<uint32_t>(q)))
-                       : make_float2(-INFINITY, 0.0f);
-#pragma unroll
-    for (int q = 0; q < 16; ++q) M = fmaxf(M, mlv[q].x);
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const float wv = (M != -INFINITY && mlv[q].y > 0.0f) ? exp2f(mlv[q].x - M) : 0.0f;
-      wgt[q] = wv;
-      L += wv * mlv[q].y;
-    }
-    cluster_sync();                    // every CTA has read the others' ml_s
-    if (tid < a.H) {
-      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-      const size_t bm = static_cast<size_t>(b) * a.M + m;
-      const float* po = a.part_o + bm * nch * kLatent * a.H + static_cast<size_t>(d0) * a.H + tid;
-      float* o = a.out + (bm * a.H + tid) * kLatent + d0;
-      for (int db = 0; db < dpc; db += 32) {
-        float acc[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          if (q >= nch || wgt[q] == 0.0f) continue;
-          const float* pc = po + static_cast<size_t>(q) * kLatent * a.H + static_cast<size_t>(db) * a.H;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) acc[i] = fmaf(wgt[q], __ldg(pc + static_cast<size_t>(i) * a.H), acc[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(o + db + i) =
-              make_float4(acc[i] * inv, acc[i + 1] * inv, acc[i + 2] * inv, acc[i + 3] * inv);
-      }
-    }
-  }
 }
 
-// out[b][m][h][d] = sum_c 2^(mx_c - M) O_c[d][h] / sum_c 2^(mx_c - M) l_c
-// One CTA per (request, way) and block of 32 dims; thread h handles head h.
-constexpr int kCombMaxCh = 64;
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
-                                                      const float2* __restrict__ part_ml,
-                                                      float* __restrict__ out, int H, int nch) {
-  const int bm = blockIdx.x;
-  const int d0 = blockIdx.y * 32;
-  const int h = threadIdx.x;
-  if (h >= H) return;
+// out[b][m][h][:] = sum_c 2^(mx_c - M) O_c[h][:] / sum_c 2^(mx_c - M) l_c over the
+// chunk partials of (request b, way m), M the running maximum (merged 16
+// chunks at a time, rescaling the running sums when M grows).  One CTA per
+// (head, request-way); thread t owns dims 4t..4t+3.  Launched as a
+// programmatic dependent of the attention kernel: it waits for that grid
+// before reading the partials.
+__global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ part_o,
+                                                    const float2* __restrict__ part_ml,
+                                                    float* __restrict__ out, int H, int nch) {
+  pdl_wait_previous();
+  const int h = blockIdx.x, bm = blockIdx.y, t = threadIdx.x;
   const float2* ml = part_ml + static_cast<size_t>(bm) * nch * H + h;
-  float wgt[kCombMaxCh];
-  float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, ml[static_cast<size_t>(c) * H].x);
-  float L = 0.0f;
-  for (int c = 0; c < nch; ++c) {
-    const float2 v = ml[static_cast<size_t>(c) * H];
-    const float wv = (M != -INFINITY && v.y > 0.0f) ? exp2f(v.x - M) : 0.0f;
-    wgt[c] = wv;
-    L += wv * v.y;
+  // float4 index of dims 4t..4t+3 of head h inside a chunk's partial
+  const int qt = t >> 5, jt = (t & 31) ^ (h & 7);
+  const float4* po = reinterpret_cast<const float4*>(part_o + static_cast<size_t>(bm) * nch * H * kLatent) +
+                     (static_cast<size_t>(qt) * H + h) * 32 + jt;
+  const size_t cstride = static_cast<size_t>(H) * (kLatent / 4);
+  float M = -INFINITY, L = 0.0f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < nch; c0 += 16) {
+    float2 e[16];
+    float4 v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int c = c0 + q;
+      e[q] = c < nch ? __ldg(ml + static_cast<size_t>(c) * H) : make_float2(-INFINITY, 0.0f);
+      v[q] = c < nch ? __ldg(po + static_cast<size_t>(c) * cstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float Mg = M;
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      if (e[q].y > 0.0f) Mg = fmaxf(Mg, e[q].x);
+    const float r = (M == -INFINITY) ? 0.0f : exp2f(M - Mg);
+    acc.x *= r;
+    acc.y *= r;
+    acc.z *= r;
+    acc.w *= r;
+    L *= r;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      if (e[q].y > 0.0f) {   // a chunk with no rows leaves no O partial
+        const float w = exp2f(e[q].x - Mg);
+        L = fmaf(w, e[q].y, L);
+        acc.x = fmaf(w, v[q].x, acc.x);
+        acc.y = fmaf(w, v[q].y, acc.y);
+        acc.z = fmaf(w, v[q].z, acc.z);
+        acc.w = fmaf(w, v[q].w, acc.w);
+      }
+    }
+    M = Mg;
   }
   const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-  const float* po = part_o + static_cast<size_t>(bm) * nch * kLatent * H + static_cast<size_t>(d0) * H + h;
-  float acc[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-  for (int c = 0; c < nch; ++c) {
-    const float wv = wgt[c];
-    if (wv == 0.0f) continue;            // also skips partials of empty chunks
-    const float* pc = po + static_cast<size_t>(c) * kLatent * H;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = fmaf(wv, __ldg(pc + static_cast<size_t>(i) * H), acc[i]);
-  }
-  float* o = out + (static_cast<size_t>(bm) * H + h) * kLatent + d0;
-#pragma unroll
-  for (int i = 0; i < 32; i += 4)
-    *reinterpret_cast<float4*>(o + i) = make_float4(acc[i] * inv, acc[i + 1] * inv, acc[i + 2] * inv,
-                                                    acc[i + 3] * inv);
+  reinterpret_cast<float4*>(out + (static_cast<size_t>(bm) * H + h) * kLatent)[t] =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
 // (a6) one warp per miss row: host row of miss_tok -> pool slot miss_slot
@@ -480,56 +469,23 @@ cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(a.nch, c.mtp, c.batch);
-  a.out = out;
-  a.fused_combine = 0;
-  // the chunks of one (request, way) form a cluster when they can: nch divides
-  // 512 into whole 32-dim slices and the device schedules clusters of nch CTAs
-  static int cluster_ok[17] = {0};   // 0 unknown, 1 yes, -1 no (per cluster size)
-  const int nch = a.nch;
-  if (nch >= 1 && nch <= 16 && (kLatent % nch) == 0 && ((kLatent / nch) % 32) == 0) {
-    if (cluster_ok[nch] == 0) {
-      cluster_ok[nch] = -1;
-      if (nch > 8)
-        cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      cudaLaunchConfig_t cfgq = {};
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = nch;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      cfgq.gridDim = grid;
-      cfgq.blockDim = dim3(kAttnThreads);
-      cfgq.dynamicSmemBytes = smem;
-      cfgq.attrs = at;
-      cfgq.numAttrs = 1;
-      int ncl = 0;
-      if (cudaOccupancyMaxActiveClusters(&ncl, attn_kernel, &cfgq) == cudaSuccess && ncl > 0)
-        cluster_ok[nch] = 1;
-      cudaGetLastError();
-    }
-    a.fused_combine = cluster_ok[nch] > 0 ? 1 : 0;
-  }
-  if (a.fused_combine) {
-    cudaLaunchConfig_t cfgl = {};
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = nch;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfgl.gridDim = grid;
-    cfgl.blockDim = dim3(kAttnThreads);
-    cfgl.dynamicSmemBytes = smem;
-    cfgl.stream = st;
-    cfgl.attrs = at;
-    cfgl.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfgl, attn_kernel, qmap, a);
-  }
   attn_kernel<<<grid, kAttnThreads, smem, st>>>(qmap, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  combine_kernel<<<dim3(c.batch * c.mtp, kLatent / 32), 128, 0, st>>>(p.scr.part_o, p.scr.part_ml,
-                                                                      out, c.mla_heads, a.nch);
-  return cudaGetLastError();
+  count_launch(p);
+  cudaLaunchConfig_t cl = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cl.gridDim = dim3(c.mla_heads, c.batch * c.mtp);
+  cl.blockDim = dim3(128);
+  cl.stream = st;
+  cl.attrs = at;
+  cl.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cl, merge_kernel, static_cast<const float*>(p.scr.part_o),
+                         static_cast<const float2*>(p.scr.part_ml), out, c.mla_heads, a.nch);
+  if (e == cudaSuccess) count_launch(p);
+  return e;
 }
 
 cudaError_t launch_stage(const ess_pool& p, int layer, const int32_t* miss_tok,
@@ -541,7 +497,9 @@ cudaError_t launch_stage(const ess_pool& p, int layer, const int32_t* miss_tok,
   stage_kernel<<<grid, 256, 0, st>>>(miss_tok, miss_slot, n_miss, L.T_dev, L.page_table,
                                      L.host_latent, L.pool, MK, c.C, c.max_T, c.page,
                                      c.max_T / c.page, p.scr.status);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch(p);
+  return e;
 }
 
 }  // namespace ess

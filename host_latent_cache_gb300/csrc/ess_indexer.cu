@@ -373,7 +373,9 @@ cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, cons
     if (e != cudaSuccess) return e;
     indexer_kernel<false><<<grid, kIdxThreads, smem, st>>>(L.kmap, qmap, a);
   }
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch(p);
+  return e;
 }
 
 }  // namespace ess

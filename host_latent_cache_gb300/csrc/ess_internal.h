@@ -96,9 +96,15 @@ struct ess_pool {
   ess::Layout lay;
   ess::Layer* layers = nullptr;
   ess::Scratch scr;
+  long long launches = 0;          // kernels launched by this pool's calls
+  long long* n_launch = nullptr;   // -> launches (copies of the handle count into it)
 };
 
 namespace ess {
+
+inline void count_launch(const ess_pool& p) {
+  if (p.n_launch) ++*p.n_launch;
+}
 
 // Kernel launchers (one per kernel file).  They assume validated arguments.
 // with_hist: also accumulate the per-(request, way) score histogram in the

@@ -963,7 +963,9 @@ cudaError_t launch_order_reset(const ess_pool& p, int layer, cudaStream_t st) {
   const ess_config& c = p.cfg;
   const int n = c.batch * c.C;
   order_reset_kernel<<<(2 * n + 255) / 256, 256, 0, st>>>(p.layers[layer].order, n, c.C);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch(p);
+  return e;
 }
 
 cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, bool hist_given,
@@ -1020,7 +1022,9 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   select_kernel<<<c.batch * CL, NT, smem, st>>>(a);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch(p);
+  return e;
 }
 
 // ---------------------------------------------------------------------------

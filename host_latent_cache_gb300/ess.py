@@ -37,7 +37,7 @@ EXPORTS = (
     "ess_indexer_topk", "ess_stage_misses", "ess_sparse_mla_decode", "ess_step",
     "ess_step_profiled", "ess_step_host",
     "ess_pipeline_step", "ess_pool_get_state", "ess_pool_set_state", "ess_pool_get_rows",
-    "ess_pool_read_stats", "ess_pool_poll",
+    "ess_pool_read_stats", "ess_pool_poll", "ess_pool_kernel_launches",
 )
 
 
@@ -102,6 +102,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "ess_pool_get_rows": [P, I, P],
         "ess_pool_read_stats": [P, I, ctypes.POINTER(ess_stats), I],
         "ess_pool_poll": [P, P],
+        "ess_pool_kernel_launches": [P, ctypes.POINTER(ctypes.c_int64)],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -288,6 +289,12 @@ def ess_pool_read_stats(pool, layer, reset: bool = False) -> ess_stats:
     s = ess_stats()
     check(load().ess_pool_read_stats(pool, layer, ctypes.byref(s), int(reset)), "ess_pool_read_stats")
     return s
+
+
+def ess_pool_kernel_launches(pool) -> int:
+    n = ctypes.c_int64(0)
+    check(load().ess_pool_kernel_launches(pool, ctypes.byref(n)), "ess_pool_kernel_launches")
+    return int(n.value)
 
 
 def ess_pool_poll(pool, stream=None) -> int:

@@ -122,6 +122,9 @@ class Session:
         ess.ess_pool_get_rows(self.pool, layer, rows)
         return rows.numpy().view(np.uint16)
 
+    def kernel_launches(self) -> int:
+        return ess.ess_pool_kernel_launches(self.pool)
+
     def stats(self, layer, reset=False):
         return ess.ess_pool_read_stats(self.pool, layer, reset)
 

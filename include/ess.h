@@ -285,6 +285,11 @@ ess_status ess_pool_get_rows(ess_pool* pool, int layer, void* rows_host);
 /* Read (and optionally zero) the per-layer counters (synchronous). */
 ess_status ess_pool_read_stats(ess_pool* pool, int layer, ess_stats* out, int reset);
 
+/* Number of CUDA kernels the calls on this pool have launched since it was
+ * created, counted on the host as each launch is enqueued (memsets and
+ * copies are not kernels and are not counted). */
+ess_status ess_pool_kernel_launches(const ess_pool* pool, int64_t* count);
+
 /* Synchronise stream, return the first device-side error since the last
  * poll (ESS_OK if none) and clear it. */
 ess_status ess_pool_poll(ess_pool* pool, ess_stream_t stream);

@@ -196,6 +196,21 @@ def test_ess_step_matches_separate_calls():
     b.close()
 
 
+def test_kernel_launch_count():
+    """A fused step launches the indexer, selection and attention (plus the
+    merge kernel when the chunks cannot form a cluster); staged adds the copy."""
+    cfg = W.tiny().replace(T=2048, k=256, C=512)
+    counts = {}
+    for mode in (ess.ESS_MISS_FUSED, ess.ESS_MISS_STAGED):
+        p = Pair(cfg, miss_mode=mode)
+        n0 = p.sess.kernel_launches()
+        p.run_step(api="step")
+        counts[mode] = p.sess.kernel_launches() - n0
+        p.close()
+    assert counts[ess.ESS_MISS_FUSED] in (3, 4)
+    assert counts[ess.ESS_MISS_STAGED] == counts[ess.ESS_MISS_FUSED] + 1
+
+
 def test_v32_shaped_reduced_batch():
     cfg = W.v32_32k().replace(batch=2, T=8192 + 64, T_per_req=[8192 + 64, 5000], steps=4)
     p = Pair(cfg)
