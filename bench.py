@@ -46,8 +46,8 @@ ROW_BYTES = 1152
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=32)
-    ap.add_argument("--warmup", type=int, default=4)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_128k", choices=sorted(W.ALL_CONFIGS))
     ap.add_argument("--miss-mode", default="fused", choices=["fused", "staged"])
@@ -118,6 +118,7 @@ class ClockSampler:
         self.samples, self.smax, self.reasons, self.power = [], None, set(), []
         self.proc = None
         self.thread = None
+        self.marks = []
 
     def _nvml(self):
         import ctypes
@@ -144,13 +145,14 @@ class ClockSampler:
             def run():
                 clk, rs, pw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
                 while not self.stop:
-                    if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                    timed = len(self.marks) == 1     # between the two marks
+                    if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and timed:
                         self.samples.append(float(clk.value))
-                    if get_reasons(h, ctypes.byref(rs)) == 0:
+                    if get_reasons(h, ctypes.byref(rs)) == 0 and timed:
                         for bit, name in _REASONS.items():
                             if rs.value & bit:
                                 self.reasons.add(name)
-                    if nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0:
+                    if nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 and timed:
                         self.power.append(pw.value / 1000.0)
                     time.sleep(0.001)
 
@@ -171,6 +173,10 @@ class ClockSampler:
             except Exception:
                 self.proc = None
         return self
+
+    def mark(self):
+        """Start (first call) and end (second call) of the timed region."""
+        self.marks.append(time.time())
 
     def __exit__(self, *a):
         self.stop = True
@@ -262,7 +268,9 @@ def measure_overlap(cfg, ld, n_steps, stream, host_buffers):
     step, and OverlapRatio = (T_copy + T_SFA - T_fused) / T_copy.  A fused pool
     runs the steps first, then a staged pool replays the same inputs from the
     same empty state (identical selections and misses), one pool at a time;
-    both read the latent cache of the main session's host buffer."""
+    both read the latent cache of the main session's host buffer.  Events
+    between the kernels stop them from launching early, as in the separate
+    calls these timings stand for."""
     import torch
     from host_latent_cache_gb300 import ess
     from host_latent_cache_gb300.session import Session
@@ -272,10 +280,14 @@ def measure_overlap(cfg, ld, n_steps, stream, host_buffers):
     res, outs = {}, {}
     for mode in (ess.ESS_MISS_FUSED, ess.ESS_MISS_STAGED):
         sess = Session(cfg, [ld], miss_mode=mode, host_buffers=host_buffers)
-        rows = []
-        for q, enc, qm in steps:
-            qd, wd, qmd = sess.device_inputs(enc, wts, qm)
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ins = [sess.device_inputs(enc, wts, qm) for (_, enc, qm) in steps]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in steps]
+        nm = torch.zeros(len(steps), dtype=torch.int64, device=sess.device)
+        torch.cuda.synchronize()
+        # the steps run back to back (no host work between them): the miss
+        # path is slower right after the GPU has been idle
+        for i, (qd, wd, qmd) in enumerate(ins):
+            e = evs[i]
             sess.indexer_topk(0, qd, wd, stream)
             e[0].record(stream)
             if mode == ess.ESS_MISS_STAGED:
@@ -283,12 +295,13 @@ def measure_overlap(cfg, ld, n_steps, stream, host_buffers):
             e[1].record(stream)
             sess.attention(0, qmd, stream=stream)
             e[2].record(stream)
-            torch.cuda.synchronize()
-            rows.append((int(sess.n_miss.sum().item()), e[0].elapsed_time(e[1]),
-                         e[1].elapsed_time(e[2])))
+            nm[i] = sess.n_miss.sum()
+        torch.cuda.synchronize()
         assert sess.poll(stream) == ess.ESS_OK
+        nmh = nm.cpu().tolist()
+        res[mode] = [(int(nmh[i]), e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]))
+                     for i, e in enumerate(evs)]
         outs[mode] = sess.out.clone()
-        res[mode] = rows
         sess.close()
     fz, sg = res[ess.ESS_MISS_FUSED], res[ess.ESS_MISS_STAGED]
     assert [r[0] for r in fz] == [r[0] for r in sg]
@@ -364,12 +377,12 @@ def bench_ours(args, cfg, rank, world, local_rank):
     mode = ess.ESS_MISS_STAGED if args.miss_mode == "staged" else ess.ESS_MISS_FUSED
     sess = Session(cfg_r, [ld], miss_mode=mode)
     qs = W.QueryStream(cfg_r)
-    n_total = args.warmup + 2 * args.steps
+    n_total = args.warmup + 3 * args.steps
     wts = W.head_weights(cfg_r, ld.w)
     dev_inputs, host_inputs = [], []
     for s in range(n_total):
         q, enc, qm = qs.next()
-        if s < args.warmup + args.steps:
+        if s < args.warmup + 2 * args.steps:
             dev_inputs.append(sess.device_inputs(enc, wts, qm))
         else:
             hq = torch.from_numpy(np.ascontiguousarray(enc).view(np.uint8)).pin_memory()
@@ -392,36 +405,52 @@ def bench_ours(args, cfg, rank, world, local_rank):
 
     def one_step(i, events=None):
         qd, wd, qmd = dev_inputs[i]
-        ess.ess_step_profiled(sess.pool, 0, qd, wd, qmd, sess.out,
-                              events if events else [None] * 4, stream)
+        if events is None:
+            ess.ess_step(sess.pool, 0, qd, wd, qmd, sess.out, stream)
+        else:
+            ess.ess_step_profiled(sess.pool, 0, qd, wd, qmd, sess.out, events, stream)
 
-    for i in range(args.warmup):
-        one_step(i)
-    torch.cuda.synchronize()
-    assert sess.poll(stream) == ess.ESS_OK
-    sess.stats(0, reset=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    launches_before = sess.kernel_launches()
+    # the clock sampler starts before the warm-up, and the timed steps follow
+    # the warm-up with nothing but the barrier and a synchronize in between:
+    # the host-memory path of the misses is slow again after the GPU idles
     with ClockSampler(local_rank) as clk:
+        for i in range(args.warmup):
+            one_step(i)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        launches_before = sess.kernel_launches()
+        clk.mark()
         t_start.record(stream)
         for i in range(nsteps):
-            one_step(args.warmup + i, ev[i])
+            one_step(args.warmup + i)
         t_end.record(stream)
         torch.cuda.synchronize()
-    launches_timed = sess.kernel_launches() - launches_before
+        clk.mark()
     if dist is not None:
         dist.barrier()
     st = sess.poll(stream)
     assert st == ess.ESS_OK, ess.status_string(st)
     elapsed_ms = t_start.elapsed_time(t_end)
+    launches_timed = sess.kernel_launches() - launches_before
+    try:
+        host_thp = sum(h.huge_page_bytes() or 0 for h in sess.host)
+    except Exception:
+        host_thp = None
+    # per-kernel durations and the step counters: the next steps again, with
+    # events between the kernels (an event between two kernels stops the next
+    # one from launching early, so these steps are kept out of the timed region)
+    sess.stats(0, reset=True)
+    for i in range(nsteps):
+        one_step(args.warmup + nsteps + i, ev[i])
+    torch.cuda.synchronize()
+    assert sess.poll(stream) == ess.ESS_OK
+    stats = sess.stats(0, reset=True)
     idx_ms = [e[0].elapsed_time(e[1]) for e in ev]
     sel_ms = [e[1].elapsed_time(e[2]) for e in ev]
     att_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    stats = sess.stats(0, reset=True)
 
     # OverlapRatio of the fused miss path: fused and staged pools stepped in
     # lockstep on the same inputs (identical state trajectories)
@@ -484,6 +513,8 @@ def bench_ours(args, cfg, rank, world, local_rank):
             "kernels_ms": {"indexer": statistics.mean(idx_ms), "select": statistics.mean(sel_ms),
                            "attention": statistics.mean(att_ms)},
             "hit_rate": stats.hits / max(stats.hits + stats.misses, 1),
+            "host_latent": {"bytes": sum(h.nbytes for h in sess.host),
+                            "huge_page_bytes": host_thp},
             "overlap": overlap,
             "e2e": {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": int(sum(x.numel() * x.element_size()

@@ -99,6 +99,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything above touched only this CTA's shared memory and TMEM
+  pdl_wait_previous();
 
   // query blocks 0..3 into the stage ring
   if (tid == 32) {
@@ -351,6 +353,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ pa
                                                     const float2* __restrict__ part_ml,
                                                     float* __restrict__ out, int H, int nch) {
   pdl_wait_previous();
+  pdl_launch_dependents();
   const int h = blockIdx.x, bm = blockIdx.y, t = threadIdx.x;
   const float2* ml = part_ml + static_cast<size_t>(bm) * nch * H + h;
   // float4 index of dims 4t..4t+3 of head h inside a chunk's partial
@@ -406,6 +409,8 @@ __global__ void __launch_bounds__(256) stage_kernel(const int32_t* __restrict__ 
                                                     const uint16_t* __restrict__ host,
                                                     uint16_t* __restrict__ pool, int MK, int C,
                                                     int T, int page, int npages, int* status) {
+  pdl_wait_previous();
+  pdl_launch_dependents();
   const int b = blockIdx.y;
   const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -469,21 +474,12 @@ cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(a.nch, c.mtp, c.batch);
-  attn_kernel<<<grid, kAttnThreads, smem, st>>>(qmap, a);
-  e = cudaGetLastError();
+  e = launch_pdl(attn_kernel, grid, dim3(kAttnThreads), smem, st, qmap, a);
   if (e != cudaSuccess) return e;
   count_launch(p);
-  cudaLaunchConfig_t cl = {};
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cl.gridDim = dim3(c.mla_heads, c.batch * c.mtp);
-  cl.blockDim = dim3(128);
-  cl.stream = st;
-  cl.attrs = at;
-  cl.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cl, merge_kernel, static_cast<const float*>(p.scr.part_o),
-                         static_cast<const float2*>(p.scr.part_ml), out, c.mla_heads, a.nch);
+  e = launch_pdl(merge_kernel, dim3(c.mla_heads, c.batch * c.mtp), dim3(128), 0, st,
+                 static_cast<const float*>(p.scr.part_o), static_cast<const float2*>(p.scr.part_ml),
+                 out, c.mla_heads, a.nch);
   if (e == cudaSuccess) count_launch(p);
   return e;
 }
@@ -494,10 +490,10 @@ cudaError_t launch_stage(const ess_pool& p, int layer, const int32_t* miss_tok,
   const Layer& L = p.layers[layer];
   const int MK = c.mtp * c.k;
   dim3 grid((MK + 7) / 8, c.batch);
-  stage_kernel<<<grid, 256, 0, st>>>(miss_tok, miss_slot, n_miss, L.T_dev, L.page_table,
-                                     L.host_latent, L.pool, MK, c.C, c.max_T, c.page,
-                                     c.max_T / c.page, p.scr.status);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e =
+      launch_pdl(stage_kernel, grid, dim3(256), 0, st, miss_tok, miss_slot, n_miss,
+                 static_cast<const int32_t*>(L.T_dev), static_cast<const int32_t*>(L.page_table),
+                 L.host_latent, L.pool, MK, c.C, c.max_T, c.page, c.max_T / c.page, p.scr.status);
   if (e == cudaSuccess) count_launch(p);
   return e;
 }

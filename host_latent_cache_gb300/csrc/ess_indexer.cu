@@ -118,6 +118,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // everything above touched only this CTA's shared memory and TMEM
+  pdl_wait_previous();
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------ producer
@@ -366,14 +369,13 @@ cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, cons
     e = cudaFuncSetAttribute(indexer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    indexer_kernel<true><<<grid, kIdxThreads, smem, st>>>(L.kmap, qmap, a);
+    e = launch_pdl(indexer_kernel<true>, dim3(grid), dim3(kIdxThreads), smem, st, L.kmap, qmap, a);
   } else {
     e = cudaFuncSetAttribute(indexer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    indexer_kernel<false><<<grid, kIdxThreads, smem, st>>>(L.kmap, qmap, a);
+    e = launch_pdl(indexer_kernel<false>, dim3(grid), dim3(kIdxThreads), smem, st, L.kmap, qmap, a);
   }
-  e = cudaGetLastError();
   if (e == cudaSuccess) count_launch(p);
   return e;
 }

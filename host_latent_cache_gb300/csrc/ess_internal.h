@@ -106,6 +106,26 @@ inline void count_launch(const ess_pool& p) {
   if (p.n_launch) ++*p.n_launch;
 }
 
+// Launches a kernel as a programmatic dependent of the previous kernel on the
+// stream: its CTAs may be scheduled before that kernel has finished, so every
+// kernel of this library waits (griddepcontrol.wait) before it touches global
+// memory, and lets its own dependents launch once it is running.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Kernel launchers (one per kernel file).  They assume validated arguments.
 // with_hist: also accumulate the per-(request, way) score histogram in the
 // pool's scratch (it must be zero; the selection kernel zeroes it after use).

@@ -298,6 +298,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     select_kernel(const SelArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];
   __shared__ SelShared sh;
+  pdl_wait_previous();
+  pdl_launch_dependents();
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
@@ -1021,8 +1023,7 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  select_kernel<<<c.batch * CL, NT, smem, st>>>(a);
-  e = cudaGetLastError();
+  e = launch_pdl(select_kernel, dim3(c.batch * CL), dim3(NT), smem, st, a);
   if (e == cudaSuccess) count_launch(p);
   return e;
 }
