@@ -292,7 +292,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         mbar_arrive(smem_u32(&acce[acc]));
         if (in_range) {
           uint32_t* hseg = hist + (seg & 1) * HB;
-          for (int m = 0; m < a.M; ++m) {
+#pragma unroll
+          for (int m = 0; m < kMaxWays; ++m) {   // unrolled: sm stays in registers
+            if (m >= a.M) break;
             const float sv = __fmul_rn(sm[m], sc) + 0.0f;  // one rounding; +0 for a zero score
             a.scores[(static_cast<size_t>(b) * a.M + m) * a.T + t] = sv;
             if (HB) atomicAdd(hseg + m * kHistBins + (float_key(sv) >> 20), 1u);

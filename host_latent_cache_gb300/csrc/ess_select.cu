@@ -96,6 +96,7 @@ struct SelShared {
   int fallback;
   int nl;
   int ncand[kMaxWays];                // this CTA's candidates per way (read through DSMEM)
+  int gcnt[CL];                       // every CTA's candidate count for the way being gathered
   int gsel;                           // 1: candidates are gathered into every CTA
   // published for the other CTAs of the cluster (read through DSMEM)
   int pub_overflow, pub_nmiss, pub_nu, pub_hit[kMaxWays], pub_miss[kMaxWays], pub_unst,
@@ -405,14 +406,25 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       int tot;
       const int excl = block_scan(s8, tot, sh, parity);
       if (excl < keff && keff <= excl + s8) {
-        int acc = excl, j = 0;
-        for (; j < 7; ++j) {
-          if (acc + c8[j] >= keff) break;
-          acc += c8[j];
+        // first of this thread's bins (descending) where the count reaches keff;
+        // unrolled so c8 stays in registers
+        int acc = excl, jsel = 7, cj = c8[7];
+        bool found = false;
+#pragma unroll
+        for (int j = 0; j < 7; ++j) {
+          if (!found) {
+            if (acc + c8[j] >= keff) {
+              found = true;
+              jsel = j;
+              cj = c8[j];
+            } else {
+              acc += c8[j];
+            }
+          }
         }
-        sh.b1[m] = kHistBins - 1 - 8 * tid - j;
+        sh.b1[m] = kHistBins - 1 - 8 * tid - jsel;
         sh.take1[m] = keff - acc;
-        sh.cand1[m] = c8[j];
+        sh.cand1[m] = cj;
       }
       if (tid == 0 && tot != Tb) sh.fallback = 1;  // histogram does not describe these scores
     }
@@ -442,7 +454,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       if (!use) lo_k[m] = hi_k[m] = 0xFFFFFFFFu;
       if (use && bin == 0xFFFu && !all_in) hi_k[m] = 0xFFFFFFFFu;  // top bin: nothing above it
     }
-    auto coarse_flags = [&](int i) -> uint32_t {
+    auto coarse_flags = [=](int i) -> uint32_t {
       uint32_t f = 0;
 #pragma unroll
       for (int m = 0; m < kMaxWays; ++m) {
@@ -521,15 +533,27 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       // exact threshold locally: the same result in every CTA, no more barriers
       for (int m = 0; m < M; ++m) {
         if (!sh.active[m]) continue;
-        int off = 0;
-        for (uint32_t r = 0; r < CL; ++r) {
-          const int n = static_cast<int>(ld_dsmem_u32(dsmem_addr(smem_u32(&sh.ncand[m]), r)));
-          const uint32_t src = dsmem_addr(smem_u32(ckey + m * lcap), r);
-          for (int i = tid; i < n && off + i < a.gcap; i += NT) {
-            gkey[off + i] = ld_dsmem_u32(src + 4u * i);
-            grank[off + i] = static_cast<uint8_t>(r);
-          }
-          off += n;
+        // every CTA's count first, then all the remote reads at once
+        if (tid < CL)
+          sh.gcnt[tid] = static_cast<int>(
+              ld_dsmem_u32(dsmem_addr(smem_u32(&sh.ncand[m]), static_cast<uint32_t>(tid))));
+        __syncthreads();
+        int roff[CL + 1];
+        roff[0] = 0;
+#pragma unroll
+        for (int r = 0; r < CL; ++r) roff[r + 1] = roff[r] + sh.gcnt[r];
+        const int off = roff[CL];
+        const int ngc = off < a.gcap ? off : a.gcap;
+        const uint32_t kbase = smem_u32(ckey + m * lcap);
+        for (int g = tid; g < ngc; g += NT) {
+          int r = 0;
+#pragma unroll
+          for (int q = 1; q < CL; ++q) r += g >= roff[q] ? 1 : 0;
+          int base = 0;
+#pragma unroll
+          for (int q = 0; q < CL; ++q) base = (q == r) ? roff[q] : base;
+          gkey[g] = ld_dsmem_u32(dsmem_addr(kbase, static_cast<uint32_t>(r)) + 4u * (g - base));
+          grank[g] = static_cast<uint8_t>(r);
         }
         __syncthreads();
         const int ng = off < a.gcap ? off : a.gcap;
@@ -622,7 +646,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         f = lflag[e];
       }
       uint32_t sel = f & 0xFu;
-      for (int m = 0; m < M; ++m) {
+#pragma unroll
+      for (int m = 0; m < kMaxWays; ++m) {
+        if (m >= M) break;
         if (!sh.active[m]) continue;
         const bool cm = (f >> (4 + m)) & 1u;
         const uint32_t k20 = cm ? (score_key(m, tok - r0) & 0xFFFFFu) : 0u;
@@ -663,7 +689,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     for (int base = 0; base < nloc; base += NT * 4) {
       const int i0 = base + tid * 4;
       uint32_t selbits[4] = {0, 0, 0, 0};
-      for (int m = 0; m < M; ++m) {
+#pragma unroll
+      for (int m = 0; m < kMaxWays; ++m) {
+        if (m >= M) break;
         const uint32_t thr = sh.prefix[m];
         bool eq[4];
         int neq = 0;
@@ -749,16 +777,31 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   {
     // unstamped entries among my positions of the list (hits were stamped)
     int cnt = 0;
-    for (int i = tid; i < cl; i += NT) {
-      int s = cslot[i];
-      if (s < 0 || s >= a.C) {
-        set_status(a.status, ESS_ERR_DEVICE_CHECK);
-        s = 0;
+    constexpr int U = 8;   // loads in flight per thread
+    for (int i0 = tid; i0 < cl; i0 += NT * U) {
+      int sv[U], lu[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * NT;
+        int sl = i < cl ? cslot[i] : 0;
+        if (sl < 0 || sl >= a.C) {
+          set_status(a.status, ESS_ERR_DEVICE_CHECK);
+          sl = 0;
+        }
+        sv[u] = sl;
       }
-      cslot[i] = s;
-      const bool u = a.last_used[bC + s] != step_b;
-      cflag[i] = u ? 1 : 0;
-      cnt += u ? 1 : 0;
+#pragma unroll
+      for (int u = 0; u < U; ++u) lu[u] = (i0 + u * NT < cl) ? a.last_used[bC + sv[u]] : step_b;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * NT;
+        if (i < cl) {
+          const bool un = lu[u] != step_b;
+          cslot[i] = sv[u];
+          cflag[i] = un ? 1 : 0;
+          cnt += un ? 1 : 0;
+        }
+      }
     }
     for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
     if (lane == 0 && cnt) atomicAdd(&sh.pub_unst, cnt);
@@ -826,10 +869,20 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   {
     // hits among my slot range (victims are not stamped yet)
     int cnt = 0;
-    for (int i = tid; i < cl; i += NT) {
-      const bool h = a.last_used[bC + p0 + i] == step_b;
-      cflag[i] = h ? 1 : 0;
-      cnt += h ? 1 : 0;
+    constexpr int U = 8;   // loads in flight per thread
+    for (int i0 = tid; i0 < cl; i0 += NT * U) {
+      int lu[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) lu[u] = (i0 + u * NT < cl) ? a.last_used[bC + p0 + i0 + u * NT] : 0;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * NT;
+        if (i < cl) {
+          const bool h = lu[u] == step_b;
+          cflag[i] = h ? 1 : 0;
+          cnt += h ? 1 : 0;
+        }
+      }
     }
     for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
     if (lane == 0 && cnt) atomicAdd(&sh.pub_stamp, cnt);
