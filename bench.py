@@ -435,10 +435,6 @@ def bench_ours(args, cfg, rank, world, local_rank):
     assert st == ess.ESS_OK, ess.status_string(st)
     elapsed_ms = t_start.elapsed_time(t_end)
     launches_timed = sess.kernel_launches() - launches_before
-    try:
-        host_thp = sum(h.huge_page_bytes() or 0 for h in sess.host)
-    except Exception:
-        host_thp = None
     # per-kernel durations and the step counters: the next steps again, with
     # events between the kernels (an event between two kernels stops the next
     # one from launching early, so these steps are kept out of the timed region)
@@ -513,8 +509,6 @@ def bench_ours(args, cfg, rank, world, local_rank):
             "kernels_ms": {"indexer": statistics.mean(idx_ms), "select": statistics.mean(sel_ms),
                            "attention": statistics.mean(att_ms)},
             "hit_rate": stats.hits / max(stats.hits + stats.misses, 1),
-            "host_latent": {"bytes": sum(h.nbytes for h in sess.host),
-                            "huge_page_bytes": host_thp},
             "overlap": overlap,
             "e2e": {"value": e2e_value, "unit": UNIT,
                     "h2d_bytes_per_step": int(sum(x.numel() * x.element_size()

@@ -1,7 +1,5 @@
 // Host side of the C ABI declared in ess.h: workspace layout, argument
 // checks, tensor-map encoding and the launch sequences of each entry point.
-#include <sys/mman.h>
-#include <unistd.h>
 
 #include <algorithm>
 #include <cstdio>
@@ -157,62 +155,22 @@ const char* ess_status_string(ess_status s) {
   return "unknown status";
 }
 
-namespace {
-struct HostMapping {
-  void* base;
-  size_t len;
-};
-std::mutex g_host_mu;
-std::unordered_map<void*, HostMapping> g_host_maps;
-
-size_t thp_size() {
-  size_t sz = 2u << 20;
-  if (FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
-    unsigned long long v = 0;
-    if (std::fscanf(f, "%llu", &v) == 1 && v >= 4096 && v <= (1ull << 30)) sz = v;
-    std::fclose(f);
-  }
-  return sz;
-}
-}  // namespace
-
 ess_status ess_host_alloc(size_t bytes, void** out) {
   if (!out || bytes == 0) return ESS_ERR_INVALID_ARG;
   *out = nullptr;
-  const size_t align = thp_size();
-  const size_t len = bytes + align;
-  void* raw = mmap(nullptr, len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
-  if (raw == MAP_FAILED) return ESS_ERR_OOM;
-  char* p = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(raw) + align - 1) &
-                                    ~static_cast<uintptr_t>(align - 1));
-  madvise(p, bytes, MADV_HUGEPAGE);  // advisory; plain pages if huge pages are unavailable
-  std::memset(p, 0, bytes);
-  if (cudaHostRegister(p, bytes, cudaHostRegisterDefault) != cudaSuccess) {
+  void* p = nullptr;
+  if (cudaHostAlloc(&p, bytes, cudaHostAllocPortable | cudaHostAllocMapped) != cudaSuccess) {
     cudaGetLastError();
-    munmap(raw, len);
-    return ESS_ERR_CUDA;
+    return ESS_ERR_OOM;
   }
-  {
-    std::lock_guard<std::mutex> g(g_host_mu);
-    g_host_maps[p] = HostMapping{raw, len};
-  }
+  std::memset(p, 0, bytes);
   *out = p;
   return ESS_OK;
 }
 
 ess_status ess_host_free(void* ptr) {
   if (!ptr) return ESS_ERR_INVALID_ARG;
-  HostMapping m;
-  {
-    std::lock_guard<std::mutex> g(g_host_mu);
-    auto it = g_host_maps.find(ptr);
-    if (it == g_host_maps.end()) return ESS_ERR_INVALID_ARG;
-    m = it->second;
-    g_host_maps.erase(it);
-  }
-  const cudaError_t e = cudaHostUnregister(ptr);
-  munmap(m.base, m.len);
-  return e == cudaSuccess ? ESS_OK : ESS_ERR_CUDA;
+  return cudaFreeHost(ptr) == cudaSuccess ? ESS_OK : ESS_ERR_CUDA;
 }
 
 ess_status ess_pool_device_bytes(const ess_config* cfg, size_t* bytes) {

@@ -141,8 +141,8 @@ def _stream(stream) -> Optional[int]:
 
 
 class HostBuffer:
-    """Host memory from ess_host_alloc (huge-page backed, registered with CUDA),
-    exposed as a numpy array; freed with close()."""
+    """Pinned, device-mapped host memory from ess_host_alloc, exposed as a
+    numpy array; freed with close()."""
 
     def __init__(self, shape, dtype):
         import numpy as np
@@ -158,24 +158,6 @@ class HostBuffer:
 
     def data_ptr(self):
         return self.ptr
-
-    def huge_page_bytes(self):
-        """Bytes of this buffer the kernel backs with transparent huge pages
-        (from /proc/self/smaps; None where that file is not readable)."""
-        try:
-            lo, hi = self.ptr, self.ptr + self.nbytes
-            total, cur = 0, None
-            with open("/proc/self/smaps") as f:
-                for line in f:
-                    head = line.split()[0]
-                    if "-" in head and ":" not in head:
-                        a, b = (int(x, 16) for x in head.split("-"))
-                        cur = (a, b) if a < hi and b > lo else None
-                    elif cur is not None and head == "AnonHugePages:":
-                        total += int(line.split()[1]) * 1024
-            return total
-        except OSError:
-            return None
 
     def close(self):
         if self.ptr:

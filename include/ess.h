@@ -126,15 +126,13 @@ ess_status ess_pool_create(const ess_config* cfg, void* dev_workspace, size_t ws
 /* Release the handle (the caller frees the workspace). */
 ess_status ess_pool_destroy(ess_pool* pool);
 
-/* Allocate host memory for a latent cache: an anonymous mapping aligned to
- * the transparent-huge-page size and advised for huge pages (fewer GPU
- * translations of host pages when misses read scattered rows), touched, and
- * registered with CUDA so that kernels can read it (pinned, mapped).  The
- * memory is zero-filled.  Release it with ess_host_free.  Errors:
- * ESS_ERR_OOM (mapping failed), ESS_ERR_CUDA (registration failed). */
+/* Allocate pinned host memory for a latent cache, mapped into the device
+ * address space (the kernels read miss rows from it directly) and usable from
+ * every device.  The memory is zero-filled.  Release it with ess_host_free.
+ * Errors: ESS_ERR_OOM (the allocation failed). */
 ess_status ess_host_alloc(size_t bytes, void** out);
 
-/* Unregister and unmap memory from ess_host_alloc. */
+/* Free memory from ess_host_alloc. */
 ess_status ess_host_free(void* ptr);
 
 /* Bind the inputs of one layer ([FO] "architecture": host master copy
