@@ -295,6 +295,9 @@ __device__ __forceinline__ void set_quota(SelShared& sh, int nw) {
   }
 }
 
+// MW: the number of MTP ways, fixed at compile time so every per-way loop over
+// the tokens unrolls to exactly the ways that exist
+template <int MW>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     select_kernel(const SelArgs a) {
   extern __shared__ __align__(16) uint8_t dsm[];
@@ -305,7 +308,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   const int lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
   const int b = blockIdx.x / CL;
-  const int M = a.M;
+  constexpr int M = MW;
   const int MK = M * a.k;
   const int Tb = a.Tb[b];
   const int keff = a.k < Tb ? a.k : Tb;
@@ -1073,10 +1076,14 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
   kb = (kb + 15) / 16 * 16;
   a.keys_bytes = static_cast<uint32_t>(kb);
   const size_t smem = kb + fixed;
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  void (*kern)(SelArgs) = c.mtp == 1 ? select_kernel<1>
+                        : c.mtp == 2 ? select_kernel<2>
+                        : c.mtp == 3 ? select_kernel<3>
+                                     : select_kernel<4>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  e = launch_pdl(select_kernel, dim3(c.batch * CL), dim3(NT), smem, st, a);
+  e = launch_pdl(kern, dim3(c.batch * CL), dim3(NT), smem, st, a);
   if (e == cudaSuccess) count_launch(p);
   return e;
 }
