@@ -471,26 +471,52 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     const int per_w = (((nloc + NW - 1) / NW) + 31) & ~31;
     const int wlo = warp * per_w;
     const int whi = wlo + per_w < nloc ? wlo + per_w : nloc;
+    // one pass: each warp stages its flagged tokens (in the candidate-key
+    // gather buffer, unused until later) and copies them to their place once
+    // the warps' counts are known; a warp whose range flags more than its
+    // staging holds lists its range a second time instead
+    constexpr int WSTAGE = 128;
+    uint32_t* stok = gkey + warp * WSTAGE;
+    uint8_t* sflg = grank + warp * WSTAGE;
     int wcnt = 0;
-    for (int base = wlo; base < whi; base += 32) {
-      const int i = base + lane;
-      const uint32_t f = i < whi ? coarse_flags(i) : 0u;
-      wcnt += __popc(__ballot_sync(0xffffffffu, f != 0));
-    }
-    int total;
-    int pos = warp_base(wcnt, total, sh);
     for (int base = wlo; base < whi; base += 32) {
       const int i = base + lane;
       const uint32_t f = i < whi ? coarse_flags(i) : 0u;
       const unsigned bal = __ballot_sync(0xffffffffu, f != 0);
       if (f) {
-        const int p = pos + __popc(bal & lt);
-        if (p < lcap) {
-          ltok[p] = r0 + i;
-          lflag[p] = static_cast<uint8_t>(f);
+        const int p = wcnt + __popc(bal & lt);
+        if (p < WSTAGE) {
+          stok[p] = static_cast<uint32_t>(r0 + i);
+          sflg[p] = static_cast<uint8_t>(f);
         }
       }
-      pos += __popc(bal);
+      wcnt += __popc(bal);
+    }
+    __syncwarp();
+    int total;
+    int pos = warp_base(wcnt, total, sh);
+    if (wcnt <= WSTAGE) {
+      for (int j = lane; j < wcnt; j += 32) {
+        const int p = pos + j;
+        if (p < lcap) {
+          ltok[p] = static_cast<int>(stok[j]);
+          lflag[p] = sflg[j];
+        }
+      }
+    } else {
+      for (int base = wlo; base < whi; base += 32) {
+        const int i = base + lane;
+        const uint32_t f = i < whi ? coarse_flags(i) : 0u;
+        const unsigned bal = __ballot_sync(0xffffffffu, f != 0);
+        if (f) {
+          const int p = pos + __popc(bal & lt);
+          if (p < lcap) {
+            ltok[p] = r0 + i;
+            lflag[p] = static_cast<uint8_t>(f);
+          }
+        }
+        pos += __popc(bal);
+      }
     }
     const int nl = total < lcap ? total : lcap;
     // candidates of each way in list order, with their low 20 key bits
@@ -573,27 +599,18 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
             if ((k & msk) == pre) atomicAdd(&H[(k >> lo) & (kDig - 1)], 1u);
           }
           __syncthreads();
-          if (warp == 0) {
-            const uint32_t* T = H + kDig - 1 - 32 * lane;
-            int s32 = 0;
-            for (int j = 0; j < 32; ++j) s32 += static_cast<int>(T[-j]);
-            int incl = s32;
-            for (int o = 1; o < 32; o <<= 1) {
-              const int y = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += y;
-            }
-            const unsigned bal = __ballot_sync(0xffffffffu, incl >= need);
-            const int L = bal ? __ffs(bal) - 1 : 31;
-            if (lane == L) {
-              const uint32_t* TL = H + kDig - 1 - 32 * L;
-              int acc = incl - s32, j = 0;
-              for (; j < 31; ++j) {
-                const int cj = static_cast<int>(TL[-j]);
-                if (acc + cj >= need) break;
-                acc += cj;
-              }
-              sh.prefix[m] = pre | (static_cast<uint32_t>(kDig - 1 - 32 * L - j) << lo);
-              sh.remaining[m] = need - acc;
+          {
+            // thread t owns bins kDig-1-2t and kDig-2-2t (descending): one
+            // block-wide prefix finds the bin where the count reaches need
+            static_assert(2 * NT == kDig, "two bins per thread");
+            const int hb = kDig - 1 - 2 * tid;
+            const int c0 = static_cast<int>(H[hb]), c1 = static_cast<int>(H[hb - 1]);
+            int tot2;
+            const int excl = block_scan(c0 + c1, tot2, sh, parity);
+            if (excl < need && need <= excl + c0 + c1) {
+              const bool upper = excl + c0 >= need;
+              sh.prefix[m] = pre | (static_cast<uint32_t>(upper ? hb : hb - 1) << lo);
+              sh.remaining[m] = need - (upper ? excl : excl + c0);
             }
           }
           __syncthreads();
