@@ -355,8 +355,10 @@ ess_status ess_sparse_mla_decode(ess_pool* pool, int layer, const void* q_mla,
   if (!layer_ok(pool, layer) || !q_mla || !topk_idx || !topk_slot || !out || !aligned16(q_mla) ||
       !aligned16(out))
     return ESS_ERR_INVALID_ARG;
+  // the caller's lists may come from anywhere: the kernel waits for all
+  // preceding work before it reads them
   return cuda_status(launch_attention(*pool, layer, q_mla, topk_idx, topk_slot, out,
-                                      pool->cfg.miss_mode == ESS_MISS_STAGED,
+                                      pool->cfg.miss_mode == ESS_MISS_STAGED, false,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -382,7 +384,9 @@ ess_status ess_step_profiled(ess_pool* pool, int layer, const void* q_idx, const
   if (staged && launch_stage(*pool, layer, r.miss_tok, r.miss_slot, r.n_miss, st) != cudaSuccess)
     return ESS_ERR_CUDA;
   if (!mark(2)) return ESS_ERR_CUDA;
-  if (launch_attention(*pool, layer, q_mla, r.topk_idx, r.topk_slot, out, staged, st) !=
+  // fused: the kernel just before is the LRU finishing kernel of the selection
+  // that wrote the lists, so the attention may start beside it
+  if (launch_attention(*pool, layer, q_mla, r.topk_idx, r.topk_slot, out, staged, !staged, st) !=
           cudaSuccess ||
       !mark(3))
     return ESS_ERR_CUDA;

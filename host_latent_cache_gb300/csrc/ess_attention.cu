@@ -50,6 +50,11 @@ struct AttnArgs {
   int B, M, H, k, nch, C, T, page, npages;
   float c2;                   // sm_scale * log2(e)
   int staged;
+  // 1: the previous kernel on the stream is the LRU finishing kernel, whose
+  // own predecessor (the selection that wrote the lists read here) completed
+  // before this grid could launch; the wait for the finishing kernel moves to
+  // the end so the two run side by side
+  int early;
 };
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -100,7 +105,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // everything above touched only this CTA's shared memory and TMEM
-  pdl_wait_previous();
+  if (!a.early) pdl_wait_previous();
 
   // query blocks 0..3 into the stage ring
   if (tid == 32) {
@@ -123,8 +128,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint16_t* src = nullptr;
   if (valid) {
     const int e = c + j * a.nch;
-    const int t = a.topk_idx[wo + e];
-    const int s = a.topk_slot[wo + e];
+    const int t = __ldcg(a.topk_idx + wo + e);     // through L2: written by the selection
+    const int s = __ldcg(a.topk_slot + wo + e);
     miss = s < 0;
     slot = miss ? ~s : s;
     int prow = t;
@@ -334,6 +339,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (tid < a.H) a.part_ml[pr * a.H + tid] = make_float2(-INFINITY, 0.0f);
   }
   if (tid == 0) bulk_wait_all();
+  if (a.early) pdl_wait_previous();   // finish only after the LRU finishing kernel
   pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
@@ -441,7 +447,7 @@ size_t attn_smem_bytes() { return 1024 + kRowsBytes + kQBytes + 24 * 8 + 16; }
 
 cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
                              const int32_t* topk_idx, const int32_t* topk_slot, float* out,
-                             bool misses_staged, cudaStream_t st) {
+                             bool misses_staged, bool early, cudaStream_t st) {
   const ess_config& c = p.cfg;
   const Layer& L = p.layers[layer];
   CUtensorMap qmap;
@@ -469,6 +475,7 @@ cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
   a.npages = c.max_T / c.page;
   a.c2 = c.sm_scale * 1.4426950408889634f;
   a.staged = misses_staged ? 1 : 0;
+  a.early = (early && !misses_staged) ? 1 : 0;
   const size_t smem = attn_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

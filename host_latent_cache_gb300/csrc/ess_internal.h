@@ -131,6 +131,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // pool's scratch (it must be zero; the selection kernel zeroes it after use).
 cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, const float* w,
                            float* scores, bool with_hist, cudaStream_t st);
+// Two kernels: the selection proper (lists, miss union, victims) and the LRU
+// finishing kernel (state rewrite, next LRU list, step counter).
 // hist_given: the indexer filled the histogram; otherwise the kernel builds it.
 cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, bool hist_given,
                           int32_t* topk_idx, int32_t* topk_slot, int32_t* n_miss_way,
@@ -138,9 +140,11 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
 cudaError_t launch_order_reset(const ess_pool& p, int layer, cudaStream_t st);
 cudaError_t launch_stage(const ess_pool& p, int layer, const int32_t* miss_tok,
                          const int32_t* miss_slot, const int32_t* n_miss, cudaStream_t st);
+// early: the kernel launched just before on st is the LRU finishing kernel
+// of the selection that wrote topk_idx / topk_slot (see AttnArgs::early)
 cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
                              const int32_t* topk_idx, const int32_t* topk_slot, float* out,
-                             bool misses_staged, cudaStream_t st);
+                             bool misses_staged, bool early, cudaStream_t st);
 cudaError_t launch_reset(const ess_pool& p, int layer, cudaStream_t st);
 
 // Encodes a 2-D tiled tensor map; returns false on failure.

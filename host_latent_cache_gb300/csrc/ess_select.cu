@@ -841,6 +841,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       const int pos = ordered_pos(f ? 1 : 0, run, sh, parity);
       if (f && pos < MK) {
         const int t = ltok[e];
+        lslot[e] = -2 - pos;   // a miss: its index in the request's miss union
         a.miss_tok[static_cast<size_t>(b) * MK + pos] = t;
         if (a.host != nullptr) {
           int prow = t;
@@ -885,90 +886,16 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       pos += __popc(bal);
     }
   }
-  __syncthreads();  // cflag (list flags) is reused below as per-slot stamped flags
-  {
-    // hits among my slot range (victims are not stamped yet)
-    int cnt = 0;
-    constexpr int U = 8;   // loads in flight per thread
-    for (int i0 = tid; i0 < cl; i0 += NT * U) {
-      int lu[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) lu[u] = (i0 + u * NT < cl) ? a.last_used[bC + p0 + i0 + u * NT] : 0;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * NT;
-        if (i < cl) {
-          const bool h = lu[u] == step_b;
-          cflag[i] = h ? 1 : 0;
-          cnt += h ? 1 : 0;
-        }
-      }
-    }
-    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if (lane == 0 && cnt) atomicAdd(&sh.pub_stamp, cnt);
-  }
   __syncthreads();
-  cluster_sync();  // [S5] victims listed
-  {
-    // victims in my slot range complete the stamped slots
-    int cnt = 0;
-    for (int i = tid; i < n_miss_total; i += NT) {
-      const int v = a.vlist[static_cast<size_t>(b) * MK + i];
-      if (v >= p0 && v < p0 + cl) {
-        cflag[v - p0] = 1;
-        ++cnt;
-      }
-    }
-    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if (lane == 0 && cnt) atomicAdd(&sh.pub_stamp, cnt);
-  }
+  cluster_sync();  // [S5] victims listed; no shared memory is read remotely after this
   if (n_miss_total > 0) {
-    // pair the i-th miss with the i-th victim, split across the cluster
+    // the i-th miss goes to the i-th victim (the state rewrite and the rest of
+    // the next LRU list are left to lru_finish_kernel)
     const int per = (n_miss_total + CL - 1) / CL;
     const int i0 = static_cast<int>(rank) * per;
     const int i1 = i0 + per < n_miss_total ? i0 + per : n_miss_total;
-    for (int i = i0 + tid; i < i1; i += NT) {
-      const int v = a.vlist[static_cast<size_t>(b) * MK + i];
-      const int t = a.miss_tok[static_cast<size_t>(b) * MK + i];
-      if (v < 0 || v >= a.C || t < 0 || t >= Tb) {
-        set_status(a.status, ESS_ERR_DEVICE_CHECK);
-        continue;
-      }
-      const int old = a.slot_token[bC + v];
-      if (old >= 0 && old < a.T) a.cache_slots[bT + old] = -1;
-      a.cache_slots[bT + t] = v;
-      a.slot_token[bC + v] = t;
-      a.last_used[bC + v] = step_b;
-      a.miss_slot[static_cast<size_t>(b) * MK + i] = v;
-    }
-  }
-  __syncthreads();
-  cluster_sync();  // [S6] new slots visible, stamped counts published
-  if (tid == 0) {
-    uint32_t before = 0;
-    sum_over_cluster(&sh.pub_stamp, rank, &before);
-    sh.stamp_before = static_cast<int>(before);
-  }
-  __syncthreads();
-  {
-    // stamped slots (hits and victims) close the next list in slot order
-    int wcnt = 0;
-    for (int base = clo; base < chi; base += 32) {
-      const int i = base + lane;
-      wcnt += __popc(__ballot_sync(0xffffffffu, i < chi && cflag[i]));
-    }
-    int total;
-    int pos = sh.unst_total - n_miss_total + sh.stamp_before + warp_base(wcnt, total, sh);
-    for (int base = clo; base < chi; base += 32) {
-      const int i = base + lane;
-      const bool f = i < chi && cflag[i];
-      const unsigned bal = __ballot_sync(0xffffffffu, f);
-      if (f) {
-        const int p = pos + __popc(bal & lt);
-        if (p < a.C) onxt[p] = p0 + i;
-      }
-      pos += __popc(bal);
-    }
+    for (int i = i0 + tid; i < i1; i += NT)
+      a.miss_slot[static_cast<size_t>(b) * MK + i] = a.vlist[static_cast<size_t>(b) * MK + i];
   }
 
   // ---------------------------------------------------------------- emit per-way lists
@@ -989,7 +916,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       const int pm = ordered_pos(fm ? 1 : 0, runm, sh, parity);
       const int ph = ordered_pos(fh ? 1 : 0, runh, sh, parity);
       if (fm && pm < a.k) {
-        const int ns = a.cache_slots[bT + t];
+        const int mi = -2 - s;
+        const int ns = (mi >= 0 && mi < n_miss_total) ? a.vlist[static_cast<size_t>(b) * MK + mi] : 0;
         a.topk_idx[wo + pm] = t;
         a.topk_slot[wo + pm] = ~ns;
       }
@@ -1002,7 +930,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   if (rank == 0 && tid == 0) {
     for (int m = 0; m < M; ++m) a.n_miss_way[b * M + m] = sh.nmw[m];
     a.n_miss[b] = n_miss_total;
-    a.step[b] = step_b + 1;
     if (a.stats) {
       long long h = 0, mi = 0;
       for (int m = 0; m < M; ++m) {
@@ -1020,11 +947,133 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
                 static_cast<unsigned long long>(n_miss_total) * kRowBytes);
     }
   }
-  __syncthreads();
-  cluster_sync();  // nobody leaves while others may read its shared memory
-  // every CTA has read the histogram: clear it for the next step
+  // every CTA read the histogram before [S3]: clear it for the next step
   if (rank == 0)
     for (int i = tid; i < M * kHistBins; i += NT) gh[i] = 0u;
+}
+
+// (a4) the rest of the LRU update, after the lists are out: each miss's
+// victim slot takes the miss (cache_slots / slot_token / last_used), the
+// stamped slots (hits and victims) close the next LRU list in slot order,
+// and the request's step counter advances.  Nothing downstream in the same
+// step reads what this kernel writes, so the attention kernel can run beside
+// it; the next step's selection reads it.
+struct LruShared {
+  int pub_stamp;       // stamped slots in this CTA's slot range (read through DSMEM)
+  int stamp_before, stamp_total;
+  int wcount[NW];
+};
+
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
+    lru_finish_kernel(const SelArgs a) {
+  pdl_wait_previous();
+  pdl_launch_dependents();
+  extern __shared__ __align__(16) uint8_t dsm[];
+  __shared__ LruShared sh;
+  uint8_t* cflag = dsm;                                        // [c_local] stamped flags
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int b = blockIdx.x / CL;
+  const int MK = a.M * a.k;
+  const int Tb = a.Tb[b];
+  const size_t bT = static_cast<size_t>(b) * a.T;
+  const size_t bC = static_cast<size_t>(b) * a.C;
+  const unsigned lt = lanemask_lt();
+  const int step_b = a.step[b];
+  const int p0 = static_cast<int>(rank) * a.c_local;
+  int cl = a.C - p0;
+  cl = cl < 0 ? 0 : (cl > a.c_local ? a.c_local : cl);
+  int32_t* onxt = a.order + (static_cast<size_t>((step_b & 1) ^ 1) * a.B + b) * a.C;
+  int n_miss_total = a.n_miss[b];
+  if (n_miss_total < 0 || n_miss_total > MK || n_miss_total > a.C) n_miss_total = 0;
+  if (tid == 0) sh.pub_stamp = 0;
+  __syncthreads();
+  {
+    // stamped slots of my range: the hits (stamped by the selection) and the
+    // victims (from the victim list; their last_used is rewritten below)
+    int cnt = 0;
+    constexpr int U = 8;   // loads in flight per thread
+    for (int i0 = tid; i0 < cl; i0 += NT * U) {
+      int lu[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) lu[u] = (i0 + u * NT < cl) ? a.last_used[bC + p0 + i0 + u * NT] : 0;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * NT;
+        if (i < cl) {
+          const bool h = lu[u] == step_b;
+          cflag[i] = h ? 1 : 0;
+          cnt += h ? 1 : 0;
+        }
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < n_miss_total; i += NT) {
+      const int v = a.vlist[static_cast<size_t>(b) * MK + i];
+      if (v >= p0 && v < p0 + cl) {
+        cflag[v - p0] = 1;
+        ++cnt;
+      }
+    }
+    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0 && cnt) atomicAdd(&sh.pub_stamp, cnt);
+  }
+  __syncthreads();
+  cluster_sync();  // [L1] every CTA has read last_used; stamped counts published
+  if (tid == 0) {
+    uint32_t before = 0;
+    sh.stamp_total = static_cast<int>(sum_over_cluster(&sh.pub_stamp, rank, &before));
+    sh.stamp_before = static_cast<int>(before);
+  }
+  if (n_miss_total > 0) {
+    // pair the i-th miss with the i-th victim, split across the cluster
+    const int per = (n_miss_total + CL - 1) / CL;
+    const int i0 = static_cast<int>(rank) * per;
+    const int i1 = i0 + per < n_miss_total ? i0 + per : n_miss_total;
+    for (int i = i0 + tid; i < i1; i += NT) {
+      const int v = a.vlist[static_cast<size_t>(b) * MK + i];
+      const int t = a.miss_tok[static_cast<size_t>(b) * MK + i];
+      if (v < 0 || v >= a.C || t < 0 || t >= Tb) {
+        set_status(a.status, ESS_ERR_DEVICE_CHECK);
+        continue;
+      }
+      const int old = a.slot_token[bC + v];
+      if (old >= 0 && old < a.T) a.cache_slots[bT + old] = -1;
+      a.cache_slots[bT + t] = v;
+      a.slot_token[bC + v] = t;
+      a.last_used[bC + v] = step_b;
+    }
+  }
+  __syncthreads();
+  {
+    // stamped slots close the next list in slot order
+    const int per_wc = (((cl + NW - 1) / NW) + 31) & ~31;
+    const int clo = warp * per_wc;
+    const int chi = clo + per_wc < cl ? clo + per_wc : cl;
+    int wcnt = 0;
+    for (int base = clo; base < chi; base += 32) {
+      const int i = base + lane;
+      wcnt += __popc(__ballot_sync(0xffffffffu, i < chi && cflag[i]));
+    }
+    if (lane == 0) sh.wcount[warp] = wcnt;
+    __syncthreads();
+    int pos = a.C - sh.stamp_total + sh.stamp_before;
+    for (int w = 0; w < warp; ++w) pos += sh.wcount[w];
+    for (int base = clo; base < chi; base += 32) {
+      const int i = base + lane;
+      const bool f = i < chi && cflag[i];
+      const unsigned bal = __ballot_sync(0xffffffffu, f);
+      if (f) {
+        const int p = pos + __popc(bal & lt);
+        if (p >= 0 && p < a.C) onxt[p] = p0 + i;
+      }
+      pos += __popc(bal);
+    }
+  }
+  __syncthreads();
+  cluster_sync();  // [L2] the stamped counts have been read everywhere
+  if (rank == 0 && tid == 0) a.step[b] = step_b + 1;
 }
 
 __global__ void order_reset_kernel(int32_t* order, int n_per_list, int C) {
@@ -1101,6 +1150,13 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(c.batch * CL), dim3(NT), smem, st, a);
+  if (e != cudaSuccess) return e;
+  count_launch(p);
+  const size_t smem_b = (static_cast<size_t>(a.c_local) + 15) / 16 * 16;
+  e = cudaFuncSetAttribute(lru_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_b));
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(lru_finish_kernel, dim3(c.batch * CL), dim3(NT), smem_b, st, a);
   if (e == cudaSuccess) count_launch(p);
   return e;
 }

@@ -197,8 +197,8 @@ def test_ess_step_matches_separate_calls():
 
 
 def test_kernel_launch_count():
-    """A fused step launches the indexer, selection and attention (plus the
-    merge kernel when the chunks cannot form a cluster); staged adds the copy."""
+    """A fused step launches the indexer, the selection, the LRU finishing
+    kernel, the attention and the merge; staged adds the copy."""
     cfg = W.tiny().replace(T=2048, k=256, C=512)
     counts = {}
     for mode in (ess.ESS_MISS_FUSED, ess.ESS_MISS_STAGED):
@@ -207,7 +207,7 @@ def test_kernel_launch_count():
         p.run_step(api="step")
         counts[mode] = p.sess.kernel_launches() - n0
         p.close()
-    assert counts[ess.ESS_MISS_FUSED] in (3, 4)
+    assert counts[ess.ESS_MISS_FUSED] == 5
     assert counts[ess.ESS_MISS_STAGED] == counts[ess.ESS_MISS_FUSED] + 1
 
 
