@@ -106,6 +106,17 @@ inline void count_launch(const ess_pool& p) {
   if (p.n_launch) ++*p.n_launch;
 }
 
+// Every kernel asks for the largest shared-memory carveout, even one that
+// uses little shared memory: the carveout an SM is given for one kernel's CTAs
+// decides whether a programmatic dependent with a large footprint (the
+// attention kernel beside the LRU finishing kernel, the indexer beside the
+// merge kernel) can be resident on that SM at the same time.
+template <typename... KArgs>
+cudaError_t prefer_max_smem(void (*kernel)(KArgs...)) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              static_cast<int>(cudaSharedmemCarveoutMaxShared));
+}
+
 // Launches a kernel as a programmatic dependent of the previous kernel on the
 // stream: its CTAs may be scheduled before that kernel has finished, so every
 // kernel of this library waits (griddepcontrol.wait) before it touches global
@@ -123,6 +134,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.stream = st;
   cfg.attrs = at;
   cfg.numAttrs = 1;
+  const cudaError_t e = prefer_max_smem(kernel);
+  if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 

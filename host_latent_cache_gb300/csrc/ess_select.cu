@@ -12,9 +12,6 @@
 //    slots; loads equal evictions so |C_b| never changes;
 //  - LIM emits the top-k slot list and copy triples (DRAM source, HBM
 //    destination, count) and puts the misses at the head of the list.
-//  Once a CTA knows which of its tokens miss, it asks L2 to prefetch their
-//  host rows, so the host-link transfer (and the GPU's first translation of
-//  those host pages) overlaps the LRU bookkeeping that follows.
 // "ESS: Latent-Cache Offload": the GPU sparse pool keeps its hot subset
 // under LRU.
 //
@@ -69,9 +66,6 @@ struct SelArgs {
   int32_t* miss_slot;         // [B][M*k]
   int32_t* n_miss;            // [B]
   int32_t* vlist;             // [B][M*k] victims in LRU order
-  const uint16_t* host;       // [B][T][576] host rows (device alias), for the miss prefetch
-  const int32_t* page_table;  // [B][T/page] or null
-  int page;
   long long* stats;           // [kStatFields]
   int* status;
   int B, M, k, T, C;
@@ -833,7 +827,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     n_miss_total = 0;
   }
   {
-    // the miss union in ascending token order; prefetch each miss row into L2
+    // the miss union in ascending token order
     int run = sh.miss_off;
     for (int base = 0; base < nu; base += NT) {
       const int e = base + tid;
@@ -843,14 +837,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         const int t = ltok[e];
         lslot[e] = -2 - pos;   // a miss: its index in the request's miss union
         a.miss_tok[static_cast<size_t>(b) * MK + pos] = t;
-        if (a.host != nullptr) {
-          int prow = t;
-          if (a.page_table)
-            prow = a.page_table[static_cast<size_t>(b) * (a.T / a.page) + t / a.page] * a.page +
-                   t % a.page;
-          if (prow >= 0 && prow < a.T)
-            bulk_prefetch_l2(a.host + (bT + prow) * kRowDim, kRowBytes);
-        }
       }
     }
   }
@@ -1114,9 +1100,6 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
   a.miss_slot = miss_slot;
   a.n_miss = n_miss;
   a.vlist = p.scr.vlist;
-  a.host = L.host_latent;
-  a.page_table = L.page_table;
-  a.page = c.page;
   a.stats = L.stats;
   a.status = p.scr.status;
   a.B = c.batch;
