@@ -3,7 +3,8 @@
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload long_128k|...] [--miss-mode fused|staged]
 
-A step is one decode step of the layer for the whole batch: indexer scores
+A step is one decode step of one layer for the whole batch (the bench runs
+the workload's first layer; a multi-layer workload counts one layer too): indexer scores
 over the GPU-resident indexer cache, exact top-k + cache_slots resolve +
 miss union + LRU update, and sparse MLA attention whose gather reads hits
 from the HBM pool and misses from pinned host memory.  The workload is the
@@ -91,7 +92,7 @@ def config_json(cfg: W.WorkloadConfig, n_gpus: int, miss_mode: str):
                     f"{cfg.idx_dim} {'e4m3' if cfg.idx_dtype == W.FP8_E4M3 else 'bf16'}, "
                     f"C={cfg.C}, MTP={cfg.mtp}, rho={cfg.rho}, cold bursts {cfg.cold_p}",
         "batch_per_gpu": cfg.batch, "T": cfg.T, "k": cfg.k, "C": cfg.C, "mtp": cfg.mtp,
-        "layers": cfg.layers, "miss_mode": miss_mode,
+        "layers": 1, "miss_mode": miss_mode,
         "l2": "inputs larger than L2 (keys read per step exceed the 129 MB L2); no flush",
         "parallelism": f"replicas x{n_gpus} (independent requests per GPU, no collective)",
     }
@@ -232,7 +233,7 @@ def run_oracle(cfg: W.WorkloadConfig, ld: W.LayerData, n_steps: int, n_req: int,
         lay.step(q.astype(np.float64), w, keyf, ld.idx_scale, qmf, latf)
         if s >= warm:
             t += time.perf_counter() - t0
-    units = n_req * cfg.mtp * cfg.layers * n_steps
+    units = n_req * cfg.mtp * n_steps          # one decode layer per step
     return units / t, t
 
 
@@ -471,7 +472,7 @@ def bench_ours(args, cfg, rank, world, local_rank):
     e2e_ms = e_start.elapsed_time(e_end)
 
     elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], dist, device="cuda")
-    units_step = cfg.batch * cfg.mtp * cfg.layers
+    units_step = cfg.batch * cfg.mtp            # one decode layer of the workload per step
     value = job_throughput(units_step, world, nsteps, elapsed_ms)
     e2e_value = job_throughput(units_step, world, nsteps, e2e_ms)
 
