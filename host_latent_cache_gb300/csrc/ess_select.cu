@@ -473,18 +473,29 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     uint32_t* stok = gkey + warp * WSTAGE;
     uint8_t* sflg = grank + warp * WSTAGE;
     int wcnt = 0;
-    for (int base = wlo; base < whi; base += 32) {
-      const int i = base + lane;
-      const uint32_t f = i < whi ? coarse_flags(i) : 0u;
-      const unsigned bal = __ballot_sync(0xffffffffu, f != 0);
-      if (f) {
-        const int p = wcnt + __popc(bal & lt);
-        if (p < WSTAGE) {
-          stok[p] = static_cast<uint32_t>(r0 + i);
-          sflg[p] = static_cast<uint8_t>(f);
-        }
+    // four 32-token groups per iteration: their score reads are in flight
+    // together (they come from global memory when the scores do not fit in
+    // shared memory)
+    for (int base = wlo; base < whi; base += 128) {
+      uint32_t f4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + 32 * u + lane;
+        f4[u] = i < whi ? coarse_flags(i) : 0u;
       }
-      wcnt += __popc(bal);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + 32 * u + lane;
+        const unsigned bal = __ballot_sync(0xffffffffu, f4[u] != 0);
+        if (f4[u]) {
+          const int p = wcnt + __popc(bal & lt);
+          if (p < WSTAGE) {
+            stok[p] = static_cast<uint32_t>(r0 + i);
+            sflg[p] = static_cast<uint8_t>(f4[u]);
+          }
+        }
+        wcnt += __popc(bal);
+      }
     }
     __syncwarp();
     int total;
