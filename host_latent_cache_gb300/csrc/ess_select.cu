@@ -473,18 +473,19 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     uint32_t* stok = gkey + warp * WSTAGE;
     uint8_t* sflg = grank + warp * WSTAGE;
     int wcnt = 0;
-    // four 32-token groups per iteration: their score reads are in flight
+    // eight 32-token groups per iteration: their score reads are in flight
     // together (they come from global memory when the scores do not fit in
     // shared memory)
-    for (int base = wlo; base < whi; base += 128) {
-      uint32_t f4[4];
+    constexpr int G = 8;
+    for (int base = wlo; base < whi; base += 32 * G) {
+      uint32_t f4[G];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < G; ++u) {
         const int i = base + 32 * u + lane;
         f4[u] = i < whi ? coarse_flags(i) : 0u;
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < G; ++u) {
         const int i = base + 32 * u + lane;
         const unsigned bal = __ballot_sync(0xffffffffu, f4[u] != 0);
         if (f4[u]) {
