@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-steps", type=int, default=48)
     ap.add_argument("--overlap-steps", type=int, default=24)
+    ap.add_argument("--miss-sweep", default=None,
+                    help="comma-separated hot-pool sizes C: print the distinct miss rows per "
+                         "step of the workload for each instead of the benchmark line")
     return ap.parse_args()
 
 
@@ -530,10 +533,54 @@ def bench_ours(args, cfg, rank, world, local_rank):
     return result, ld
 
 
+def miss_sweep(args, cfg):
+    """Distinct miss rows per step (after the first fill) for each hot-pool
+    size C, on the same seeded query stream, through the CUDA path.  The
+    FlashOffloading analysis reports how misses fall as the hot cache grows
+    (section "evaluation", the miss-versus-cache-size figure)."""
+    import torch
+    from host_latent_cache_gb300 import ess
+    from host_latent_cache_gb300.session import Session
+    ess.load()
+    ld = W.gen_layer(cfg)
+    sizes = [int(x) for x in args.miss_sweep.split(",")]
+    hb = [ess.HostBuffer(ld.host_latent.shape, np.uint16)]
+    hb[0].array[...] = ld.host_latent
+    res = {}
+    for C in sizes:
+        c2 = cfg.replace(C=C)
+        sess = Session(c2, [ld], host_buffers=hb)
+        qs = W.QueryStream(c2)
+        wts = W.head_weights(c2, ld.w)
+        stream = torch.cuda.current_stream()
+        for s in range(args.steps):
+            _, enc, qm = qs.next()
+            qd, wd, qmd = sess.device_inputs(enc, wts, qm)
+            if s == 1:
+                torch.cuda.synchronize()
+                sess.stats(0, reset=True)      # the first step fills the empty pool
+            ess.ess_step(sess.pool, 0, qd, wd, qmd, sess.out, stream)
+        torch.cuda.synchronize()
+        assert sess.poll(stream) == ess.ESS_OK
+        st = sess.stats(0, reset=True)
+        res[C] = st.miss_rows / max(1, args.steps - 1) / cfg.batch
+        sess.close()
+    hb[0].close()
+    line = {"miss_sweep": {"workload": cfg.name, "steps_after_first_fill": args.steps - 1,
+                           "C": sizes,
+                           "miss_rows_per_request_step": [res[c] for c in sizes],
+                           "reduction_vs_first": [1.0 - res[c] / res[sizes[0]] if res[sizes[0]]
+                                                  else None for c in sizes]}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
     cfg = W.ALL_CONFIGS[args.workload]()
+    if args.miss_sweep:
+        return miss_sweep(args, cfg) if rank == 0 else 0
     if args.impl == "reference":
         return bench_reference(args, cfg, rank, world)
     result, ld = bench_ours(args, cfg, rank, world, local_rank)
