@@ -67,7 +67,7 @@ Layout compute_layout(const ess_config& c) {
   L.o_nmiss = o;    o = align256(o + B * 4);
   L.o_vict = o;     o = align256(o + B * M * k * 4);
   L.o_hist = o;     o = align256(o + B * M * kHistBins * 4);
-  L.o_po = o;       o = align256(o + B * M * L.nch * H * kLatent * 4);
+  L.o_po = o;       o = align256(o + B * M * L.nch * H * kLatent * 2);
   L.o_pml = o;      o = align256(o + B * M * L.nch * H * 8);
   L.o_hq = o;       o = align256(o + B * M * HI * kKeyRowBytes);
   L.o_hw = o;       o = align256(o + B * M * HI * 4);
@@ -235,7 +235,7 @@ ess_status ess_pool_create(const ess_config* cfg, void* dev_workspace, size_t ws
   r.n_miss = reinterpret_cast<int32_t*>(p->ws + L.o_nmiss);
   r.vlist = reinterpret_cast<int32_t*>(p->ws + L.o_vict);
   r.ghist = reinterpret_cast<uint32_t*>(p->ws + L.o_hist);
-  r.part_o = reinterpret_cast<float*>(p->ws + L.o_po);
+  r.part_o = reinterpret_cast<uint16_t*>(p->ws + L.o_po);
   r.part_ml = reinterpret_cast<float2*>(p->ws + L.o_pml);
   r.h_qidx = reinterpret_cast<uint8_t*>(p->ws + L.o_hq);
   r.h_w = reinterpret_cast<float*>(p->ws + L.o_hw);

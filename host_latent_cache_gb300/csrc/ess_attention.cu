@@ -44,7 +44,7 @@ struct AttnArgs {
   const int32_t* page_table;  // [B][T/page] or null
   uint16_t* pool;             // [B][C][576]
   const uint16_t* host;       // [B][T][576] (device alias of pinned host memory)
-  float* part_o;              // [B][M][nch][H][512]
+  uint16_t* part_o;           // [B][M][nch][H][512] fp16 (unit u of head h at u ^ (h & 7))
   float2* part_ml;            // [B][M][nch][H]
   int* status;
   int B, M, H, k, nch, C, T, page, npages;
@@ -298,41 +298,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const bool all_o = __syncthreads_and(o_ok ? 1 : 0) != 0;
   const size_t pr = (static_cast<size_t>(b) * a.M + m) * a.nch + c;
   if (all_o) {
-    // O leaves TMEM through shared memory (the row blocks are free once PV is
-    // done), one 128-dim quarter at a time in two alternating 64 KB buffers:
-    // partial layout [quarter][head][128 dims], the float4 index j of a head's
-    // quarter stored at j ^ (head & 7) so the shared-memory writes spread over
-    // every bank
+    // O leaves TMEM through shared memory as fp16 (the row blocks are free
+    // once PV is done): [head][512 dims], the 16-byte unit u (8 dims) of head h
+    // stored at u ^ (h & 7) so the shared-memory writes spread over every bank,
+    // then one bulk copy writes the CTA's partial out.  The unnormalised sums
+    // are bounded by the row count times the largest latent value, far inside
+    // fp16 range; the merge weights and the final output stay fp32.
     tc_fence_after();
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float* po = a.part_o + pr * a.H * kLatent;
-    const uint32_t qbytes = static_cast<uint32_t>(a.H) * 128u * 4u;
-    for (int q = 0; q < 4; ++q) {
-      uint8_t* buf = rows + (q & 1) * 65536;
-      if (q >= 2) {
-        if (tid == 0) bulk_wait_read<1>();   // the copy issued from buf two quarters ago
-        __syncthreads();
-      }
-      if (warp * 32 < a.H) {   // tcgen05.ld is warp-wide: the condition is per warp
-        for (int cc = 0; cc < 4; ++cc) {
-          float v[32];
-          tmem_ld32(trow + q * 128 + cc * 32, v);
-          if (tid < a.H) {
+    if (warp * 32 < a.H) {   // tcgen05.ld is warp-wide: the condition is per warp
+      for (int cc = 0; cc < kLatent / 32; ++cc) {
+        float v[32];
+        tmem_ld32(trow + cc * 32, v);
+        if (tid < a.H) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int jj = cc * 8 + e;
-              *reinterpret_cast<float4*>(buf + tid * 512 + ((jj ^ (tid & 7)) << 4)) =
-                  make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const int u = cc * 4 + e;
+            uint4 pk;
+            pk.x = half2_bits(v[8 * e + 0], v[8 * e + 1]);
+            pk.y = half2_bits(v[8 * e + 2], v[8 * e + 3]);
+            pk.z = half2_bits(v[8 * e + 4], v[8 * e + 5]);
+            pk.w = half2_bits(v[8 * e + 6], v[8 * e + 7]);
+            *reinterpret_cast<uint4*>(rows + tid * (kLatent * 2) + ((u ^ (tid & 7)) << 4)) = pk;
           }
         }
       }
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        bulk_store(po + static_cast<size_t>(q) * a.H * 128, smem_u32(buf), qbytes);
-        bulk_commit();
-      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_store(a.part_o + pr * a.H * kLatent, smem_u32(rows),
+                 static_cast<uint32_t>(a.H) * kLatent * 2u);
+      bulk_commit();
     }
     if (tid < a.H) a.part_ml[pr * a.H + tid] = make_float2(mx, l);
   } else {
@@ -355,28 +352,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // (head, request-way); thread t owns dims 4t..4t+3.  Launched as a
 // programmatic dependent of the attention kernel: it waits for that grid
 // before reading the partials.
-__global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ part_o,
+__global__ void __launch_bounds__(128) merge_kernel(const uint16_t* __restrict__ part_o,
                                                     const float2* __restrict__ part_ml,
                                                     float* __restrict__ out, int H, int nch) {
   pdl_wait_previous();
   pdl_launch_dependents();
   const int h = blockIdx.x, bm = blockIdx.y, t = threadIdx.x;
   const float2* ml = part_ml + static_cast<size_t>(bm) * nch * H + h;
-  // float4 index of dims 4t..4t+3 of head h inside a chunk's partial
-  const int qt = t >> 5, jt = (t & 31) ^ (h & 7);
-  const float4* po = reinterpret_cast<const float4*>(part_o + static_cast<size_t>(bm) * nch * H * kLatent) +
-                     (static_cast<size_t>(qt) * H + h) * 32 + jt;
-  const size_t cstride = static_cast<size_t>(H) * (kLatent / 4);
+  // dims 4t..4t+3 of head h: half of the 16-byte unit t/2, stored at unit (t/2) ^ (h & 7)
+  const int u = (t >> 1) ^ (h & 7);
+  const uint2* po = reinterpret_cast<const uint2*>(
+      part_o + (static_cast<size_t>(bm) * nch * H + h) * kLatent + u * 8 + (t & 1) * 4);
+  const size_t cstride = static_cast<size_t>(H) * (kLatent / 4);   // one chunk, in uint2 units
   float M = -INFINITY, L = 0.0f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int c0 = 0; c0 < nch; c0 += 16) {
     float2 e[16];
-    float4 v[16];
+    uint2 v[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
       const int c = c0 + q;
       e[q] = c < nch ? __ldg(ml + static_cast<size_t>(c) * H) : make_float2(-INFINITY, 0.0f);
-      v[q] = c < nch ? __ldg(po + static_cast<size_t>(c) * cstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[q] = c < nch ? __ldg(po + static_cast<size_t>(c) * cstride) : make_uint2(0u, 0u);
     }
     float Mg = M;
 #pragma unroll
@@ -392,11 +389,12 @@ __global__ void __launch_bounds__(128) merge_kernel(const float* __restrict__ pa
     for (int q = 0; q < 16; ++q) {
       if (e[q].y > 0.0f) {   // a chunk with no rows leaves no O partial
         const float w = exp2f(e[q].x - Mg);
+        const float2 lo = half2_bits_to_float2(v[q].x), hi = half2_bits_to_float2(v[q].y);
         L = fmaf(w, e[q].y, L);
-        acc.x = fmaf(w, v[q].x, acc.x);
-        acc.y = fmaf(w, v[q].y, acc.y);
-        acc.z = fmaf(w, v[q].z, acc.z);
-        acc.w = fmaf(w, v[q].w, acc.w);
+        acc.x = fmaf(w, lo.x, acc.x);
+        acc.y = fmaf(w, lo.y, acc.y);
+        acc.z = fmaf(w, hi.x, acc.z);
+        acc.w = fmaf(w, hi.y, acc.w);
       }
     }
     M = Mg;
@@ -485,7 +483,7 @@ cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
   if (e != cudaSuccess) return e;
   count_launch(p);
   e = launch_pdl(merge_kernel, dim3(c.mla_heads, c.batch * c.mtp), dim3(128), 0, st,
-                 static_cast<const float*>(p.scr.part_o), static_cast<const float2*>(p.scr.part_ml),
+                 static_cast<const uint16_t*>(p.scr.part_o), static_cast<const float2*>(p.scr.part_ml),
                  out, c.mla_heads, a.nch);
   if (e == cudaSuccess) count_launch(p);
   return e;

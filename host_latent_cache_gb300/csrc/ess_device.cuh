@@ -118,6 +118,15 @@ __device__ __forceinline__ void pdl_wait_previous() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// fp16 pairs as raw bits (round to nearest even) and back.
+__device__ __forceinline__ uint32_t half2_bits(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t bits) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&bits));
+}
+
 // 2^x by the hardware approximation (relative error about 2^-22).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -64,7 +64,7 @@ struct Scratch {
   int32_t* n_miss = nullptr;      // [B]
   int32_t* vlist = nullptr;       // [B][M*k] victims in LRU order
   uint32_t* ghist = nullptr;      // [B][M][kHistBins] score histogram
-  float* part_o = nullptr;        // [B][M][nch][H][512]
+  uint16_t* part_o = nullptr;     // [B][M][nch][H][512] fp16, 16-byte units XOR-swizzled by head
   float2* part_ml = nullptr;      // [B][M][nch][H]
   uint8_t* h_qidx = nullptr;      // staging for ess_step_host
   float* h_w = nullptr;

@@ -51,7 +51,7 @@ def test_device_bytes_matches_layout(lib):
     n = ess.ess_pool_device_bytes(ess_config_of(cfg))
     B_, T, C, M, k, H = 8, 131072, 32768, 1, 2048, 128
     state = B_ * T * 4 + 2 * B_ * C * 4 + B_ * C * 1152
-    partials = B_ * M * (k // 128) * H * 512 * 4
+    partials = B_ * M * (k // 128) * H * 512 * 2      # fp16 chunk partials
     assert state + partials < n < state + partials + 64 * 2 ** 20
 
 
