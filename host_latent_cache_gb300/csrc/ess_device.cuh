@@ -134,10 +134,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Asynchronous prefetch of `bytes` (multiple of 16, 16-B aligned) into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 // ---------------------------------------------------------------- cp.async (16 B)
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {

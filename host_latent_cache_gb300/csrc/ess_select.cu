@@ -312,7 +312,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   float* keys_s = reinterpret_cast<float*>(dsm);                      // [M][n_local]
   int* ltok = reinterpret_cast<int*>(dsm + a.keys_bytes);             // [lcap] token list
   int* lslot = ltok + a.lcap;                                         // [lcap] resolved slot
-  int* cslot = lslot + a.lcap;                                        // [c_local] list prefetch
+  int* cslot = lslot + a.lcap;                                        // [c_local] this CTA's LRU list slice
   uint32_t* ckey = reinterpret_cast<uint32_t*>(cslot + a.c_local);    // [M][lcap] candidate keys
   uint32_t* gkey = ckey + M * a.lcap;                                 // [gcap] gathered keys
   uint8_t* grank = reinterpret_cast<uint8_t*>(gkey + a.gcap);         // [gcap] source rank
