@@ -216,6 +216,25 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, else implementer/part ids)."""
+    try:
+        name, impl, part = None, None, None
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k, v = k.strip(), v.strip()
+                if k == "model name" and not name:
+                    name = v
+                elif k == "CPU implementer" and not impl:
+                    impl = v
+                elif k == "CPU part" and not part:
+                    part = v
+        return name or (f"implementer {impl} part {part}" if impl else "unknown")
+    except OSError:
+        return "unknown"
+
+
 def run_oracle(cfg: W.WorkloadConfig, ld: W.LayerData, n_steps: int, n_req: int,
                warm: int = 1):
     """Times the CPU oracle on the first n_req requests for n_steps steps
@@ -256,7 +275,8 @@ def bench_reference(args, cfg, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
         "config": config_json(cfg, args.gpus, args.miss_mode),
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": _CORES, "kind": "oracle",
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": _CORES, "cpu": cpu_model(),
+                         "kind": "oracle",
                          "sample": f"{n_req} of {cfg.batch} requests per step, {steps} steps "
                                    f"after warm-up, float64 numpy with {_CORES} BLAS threads"},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -589,7 +609,7 @@ def main():
             n_req = min(cfg.batch, 8)
             v, t = run_oracle(cfg, ld, max(1, args.cpu_steps), n_req)
             result["cpu_baseline"] = {
-                "value": v, "unit": UNIT, "cores": _CORES, "kind": "oracle",
+                "value": v, "unit": UNIT, "cores": _CORES, "cpu": cpu_model(), "kind": "oracle",
                 "sample": f"{n_req} requests x {args.cpu_steps} steps of the same workload "
                           f"after one warm-up step ({t:.1f} s), float64 numpy, "
                           f"{_CORES} BLAS threads"}
