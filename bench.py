@@ -2,6 +2,7 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload long_128k|...] [--miss-mode fused|staged]
+                [--miss-sweep C1,C2,...]
 
 A step is one decode step of one layer for the whole batch (the bench runs
 the workload's first layer; a multi-layer workload counts one layer too): indexer scores
@@ -13,8 +14,13 @@ long-context layer: 8 requests x 131072 tokens, top-2048, 128 MLA heads,
 cold-miss bursts.  Inputs are seeded synthetic data; the keys read per step
 (138 MB) exceed the 129 MB L2, so no flush is inserted between steps.
 
+The timed steps are plain ess_step calls (each kernel launched as a
+programmatic dependent of the previous one); per-kernel durations come from
+as many further steps with events between the kernels.
+
 One JSON line is printed by rank 0.  --impl reference times the CPU oracle
-(float64 numpy) on the same workload instead.
+(float64 numpy) on the same workload instead; --miss-sweep prints the
+distinct misses per step for several hot-pool sizes instead.
 """
 from __future__ import annotations
 

@@ -175,7 +175,9 @@ ess_status ess_indexer_scores(ess_pool* pool, int layer, const void* q_idx, cons
  *               host row of miss_tok -> pool slot miss_slot, one row each)
  *   n_miss      int32 [B]: |Miss_b|
  * State: cache_slots, slot_token, last_used and step of the layer are
- * updated; entries past the selected count are left untouched. */
+ * updated; entries past the selected count are left untouched.
+ * Two kernels on stream: the selection (lists, miss union, victims) and the
+ * LRU finishing kernel (the state rewrite and the next LRU order). */
 ess_status ess_select_manage(ess_pool* pool, int layer, const float* scores,
                              int32_t* topk_idx, int32_t* topk_slot, int32_t* n_miss_way,
                              int32_t* miss_tok, int32_t* miss_slot, int32_t* n_miss,
@@ -235,14 +237,20 @@ ess_status ess_sparse_mla_decode(ess_pool* pool, int layer, const void* q_mla,
 /* (a1)-(a6) One decode step of one layer with every intermediate in the
  * pool's scratch: indexer, selection and management, (staging,) attention.
  *   q_idx, w  as in ess_indexer_scores;  q_mla, out as in
- *   ess_sparse_mla_decode. */
+ *   ess_sparse_mla_decode.
+ * Each kernel is launched as a programmatic dependent of the one before it on
+ * the stream: its prologue overlaps the previous kernel, and it waits for that
+ * kernel before touching memory.  With fused misses the attention kernel runs
+ * beside the LRU finishing kernel (it reads only the lists the selection kernel
+ * has already completed) and finishes only after it. */
 ess_status ess_step(ess_pool* pool, int layer, const void* q_idx, const float* w,
                     const void* q_mla, float* out, ess_stream_t stream);
 
 /* ess_step with measurement hooks: the same launches as ess_step, and
  * events[i] (each a cudaEvent_t, or NULL to skip) is recorded on stream
  * before the indexer (0), after the indexer (1), after selection and
- * staging (2) and after attention (3). */
+ * staging (2) and after attention and merge (3).  A recorded event between two
+ * kernels makes the second an ordinary launch (no early start). */
 ess_status ess_step_profiled(ess_pool* pool, int layer, const void* q_idx, const float* w,
                              const void* q_mla, float* out, ess_stream_t stream,
                              void* const* events);
