@@ -61,6 +61,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-steps", type=int, default=48)
     ap.add_argument("--overlap-steps", type=int, default=24)
+    ap.add_argument("--pipeline", type=int, default=0,
+                    help="time L layers of the workload as two micro-batches (half the "
+                         "requests each) on two streams against the same work on one stream")
     ap.add_argument("--miss-sweep", default=None,
                     help="comma-separated hot-pool sizes C: print the distinct miss rows per "
                          "step of the workload for each instead of the benchmark line")
@@ -601,12 +604,87 @@ def miss_sweep(args, cfg):
     return 0
 
 
+def pipeline_bench(args, cfg):
+    """The layer-wise pipeline (ess_pipeline_step): two micro-batches, half of
+    the workload's requests each, every layer on its own stream per
+    micro-batch, so one micro-batch's kernels fill the SMs the other leaves
+    idle.  Timed against the same launches issued on a single stream."""
+    import torch
+    from host_latent_cache_gb300 import ess
+    from host_latent_cache_gb300.session import Session
+    ess.load()
+    L = args.pipeline
+    half = cfg.batch // 2
+    cfgs = [cfg.replace(layers=L, batch=half, seed=cfg.seed + 100 * h) for h in range(2)]
+    sess, ins = [], []
+    for c in cfgs:
+        lds = [W.gen_layer(c, l) for l in range(L)]
+        s_ = Session(c, lds)
+        qs = [W.QueryStream(c, l) for l in range(L)]
+        steps = []
+        for _ in range(2 * (args.warmup + args.steps)):
+            per = []
+            for l in range(L):
+                _, enc, qm = qs[l].next()
+                per.append(s_.device_inputs(enc, W.head_weights(c, lds[l].w), qm))
+            steps.append(per)
+        outs = [torch.zeros((c.batch, c.mtp, c.mla_heads, 512), dtype=torch.float32,
+                            device="cuda") for _ in range(L)]
+        sess.append((s_, outs))
+        ins.append(steps)
+        del lds
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    main_st = torch.cuda.current_stream()
+
+    def run(step, two):
+        if two:
+            ess.ess_pipeline_step([s_[0].pool for s_ in sess], L,
+                                  [ins[h][step][l][0] for h in range(2) for l in range(L)],
+                                  [ins[h][step][l][1] for h in range(2) for l in range(L)],
+                                  [ins[h][step][l][2] for h in range(2) for l in range(L)],
+                                  [sess[h][1][l] for h in range(2) for l in range(L)], streams)
+        else:
+            for l in range(L):
+                for h in range(2):
+                    qd, wd, qmd = ins[h][step][l]
+                    ess.ess_step(sess[h][0].pool, l, qd, wd, qmd, sess[h][1][l], main_st)
+
+    res = {}
+    nxt = 0   # every call takes the next step's inputs
+    for mode, two in (("one_stream", False), ("two_streams", True)):
+        for _ in range(args.warmup):
+            run(nxt, two)
+            nxt += 1
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            run(nxt, two)
+            nxt += 1
+        torch.cuda.synchronize()
+        res[mode] = (time.perf_counter() - t0) / args.steps
+    for s_, _ in sess:
+        assert s_.poll() == ess.ESS_OK
+        s_.close()
+    units = cfg.batch * cfg.mtp * L
+    line = {"pipeline": {"workload": cfg.name, "layers": L, "micro_batches": 2,
+                         "requests_per_micro_batch": half, "steps": args.steps,
+                         "timing": "host wall clock between synchronizes, per step of all layers",
+                         "one_stream_us_per_step": 1e6 * res["one_stream"],
+                         "two_streams_us_per_step": 1e6 * res["two_streams"],
+                         "one_stream_token_layers_per_s": units / res["one_stream"],
+                         "two_streams_token_layers_per_s": units / res["two_streams"]}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
     cfg = W.ALL_CONFIGS[args.workload]()
     if args.miss_sweep:
         return miss_sweep(args, cfg) if rank == 0 else 0
+    if args.pipeline:
+        return pipeline_bench(args, cfg) if rank == 0 else 0
     if args.impl == "reference":
         return bench_reference(args, cfg, rank, world)
     result, ld = bench_ours(args, cfg, rank, world, local_rank)
