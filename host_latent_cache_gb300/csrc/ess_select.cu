@@ -93,12 +93,11 @@ struct SelShared {
   int gcnt[CL];                       // every CTA's candidate count for the way being gathered
   int gsel;                           // 1: candidates are gathered into every CTA
   // published for the other CTAs of the cluster (read through DSMEM)
-  int pub_overflow, pub_nmiss, pub_nu, pub_hit[kMaxWays], pub_miss[kMaxWays], pub_unst,
-      pub_stamp;
+  int pub_overflow, pub_nmiss, pub_nu, pub_hit[kMaxWays], pub_miss[kMaxWays], pub_unst;
   // cluster-wide values derived from the publications
   int n_miss_total, nu_total, miss_off, hit_off[kMaxWays], wmiss_off[kMaxWays], nmw[kMaxWays];
   int hits_total[kMaxWays];
-  int unst_before, unst_total, stamp_before;
+  int unst_before, unst_total;
   int step_b;
   unsigned long long bar;
 };
@@ -330,7 +329,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     sh.step_b = a.step[b];  // (also read directly as step0)
     sh.nl = 0;
     sh.fallback = 0;
-    sh.pub_overflow = sh.pub_nmiss = sh.pub_nu = sh.pub_unst = sh.pub_stamp = 0;
+    sh.pub_overflow = sh.pub_nmiss = sh.pub_nu = sh.pub_unst = 0;
     for (int m = 0; m < kMaxWays; ++m) {
       sh.pub_hit[m] = sh.pub_miss[m] = 0;
       sh.active[m] = 0;
