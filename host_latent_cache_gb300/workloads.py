@@ -154,6 +154,7 @@ class WorkloadConfig:
     cold_p: float = 0.0         # per (request, step >= 1) chance of a fresh query
     seed: int = 1000
     T_per_req: Optional[List[int]] = None   # ragged contexts (defaults to T for all)
+    grow: int = 0               # tokens appended to every request, one per step
     sm_scale: float = float(np.float32(1.0 / np.sqrt(576.0)))
 
     def t_of(self, b: int) -> int:
@@ -208,13 +209,18 @@ def _rng(seed: int, *ids: int) -> np.random.Generator:
 class LayerData:
     """Static inputs of one layer.
 
-    idx_keys   uint8 [B][T_max][row_bytes] (e4m3 bytes, or bf16 bits viewed as bytes)
-    idx_scale  float32 [B][T_max]   (all ones for bf16 keys)
+    idx_keys   uint8 [B][T_max][row_bytes] (e4m3 bytes, or bf16 bits viewed as bytes);
+               rows t >= T_b are zero
+    idx_scale  float32 [B][T_max]   (all ones for bf16 keys; 1 for t >= T_b)
     w          float32 [B][H_I]     head weights, on (1/64)Z in [0, 1)
     latent     uint16 [B][T_max][576] bf16 bits, LOGICAL token order
     host_latent uint16 [B][T_max][576] bf16 bits, page-permuted host layout
     page_table int32 [B][T_max / page]
     T          int32 [B]
+    With cfg.grow > 0 (decode append) the rows of the tokens appended later
+    are held apart: their keys in app_keys [B][grow][row_bytes] and
+    app_scale [B][grow]; latent holds them in logical order; host_latent has
+    zeros there (the library writes them back as their pages complete).
     """
     idx_keys: np.ndarray
     idx_scale: np.ndarray
@@ -223,10 +229,12 @@ class LayerData:
     host_latent: np.ndarray
     page_table: np.ndarray
     T: np.ndarray
+    app_keys: Optional[np.ndarray] = None
+    app_scale: Optional[np.ndarray] = None
 
 
 def t_max_of(cfg: WorkloadConfig) -> int:
-    tm = max(cfg.t_of(b) for b in range(cfg.batch))
+    tm = max(cfg.t_of(b) + cfg.grow for b in range(cfg.batch))
     tm = max(tm, 1)
     return ((tm + cfg.page - 1) // cfg.page) * cfg.page
 
@@ -234,7 +242,7 @@ def t_max_of(cfg: WorkloadConfig) -> int:
 def gen_keys(cfg: WorkloadConfig, layer: int, b: int, T_max: int):
     """Keys of one request: (bytes [T_max][row_bytes], scale [T_max])."""
     rng = _rng(cfg.seed, _TID_KEYS, layer, b)
-    T = cfg.t_of(b)
+    T = cfg.t_of(b) + cfg.grow      # rows that ever hold a token
     d = cfg.idx_dim
     x = rng.standard_normal((T_max, d), dtype=np.float32)
     if cfg.idx_dtype == FP8_E4M3:
@@ -284,7 +292,46 @@ def gen_layer(cfg: WorkloadConfig, layer: int = 0, want_latent: bool = True) -> 
             phys = pages[b][t // cfg.page] * cfg.page + (t % cfg.page)
             host[b][phys] = latent[b]
     Ts = np.array([cfg.t_of(b) for b in range(B)], dtype=np.int32)
-    return LayerData(keys, scale, w, latent, host, pages, Ts)
+    app_keys = app_scale = None
+    if cfg.grow > 0:
+        app_keys = np.zeros((B, cfg.grow, rb), dtype=np.uint8)
+        app_scale = np.ones((B, cfg.grow), dtype=np.float32)
+        for b in range(B):
+            T = int(Ts[b])
+            app_keys[b] = keys[b, T:T + cfg.grow]
+            app_scale[b] = scale[b, T:T + cfg.grow]
+            keys[b, T:] = 0
+            scale[b, T:] = 1.0
+            if want_latent:
+                t = np.arange(T, T_max)
+                host[b][pages[b][t // cfg.page] * cfg.page + t % cfg.page] = 0
+    return LayerData(keys, scale, w, latent, host, pages, Ts, app_keys, app_scale)
+
+
+def appended_token(cfg: WorkloadConfig, ld: LayerData, i: int):
+    """Inputs of the i-th decode append (token T_b + i of each request):
+    latent rows uint16 [B][576], key rows uint8 [B][row_bytes], scales
+    float32 [B]."""
+    B = cfg.batch
+    lat = np.stack([ld.latent[b, int(ld.T[b]) + i] for b in range(B)])
+    return (np.ascontiguousarray(lat), np.ascontiguousarray(ld.app_keys[:, i]),
+            np.ascontiguousarray(ld.app_scale[:, i]))
+
+
+def append_ragged() -> WorkloadConfig:
+    """Decode with appends: two ragged requests whose first pages are
+    partial, growing by 150 tokens (several pages complete and leave the
+    two-page ring)."""
+    return WorkloadConfig("append_ragged", layers=1, batch=2, T=4000, steps=150, idx_heads=4,
+                          idx_dim=64, idx_dtype=BF16, k=256, mla_heads=16, C=1024, rho=0.9,
+                          seed=1006, T_per_req=[4000, 2500], grow=150)
+
+
+def append_fp8() -> WorkloadConfig:
+    """Decode with appends on the FP8 indexer and 128 MLA heads."""
+    return WorkloadConfig("append_fp8", layers=1, batch=2, T=3000, steps=140, idx_heads=64,
+                          idx_dim=128, idx_dtype=FP8_E4M3, k=512, mla_heads=128, C=1024,
+                          rho=0.9, seed=1007, T_per_req=[3000, 2100], grow=140)
 
 
 # --------------------------------------------------------------------------

@@ -17,6 +17,7 @@ path computes, in float64 where the arithmetic is floating point:
    (lru_update)
 5. absorbed-MLA softmax attention over the selected latent rows, read
    straight from the full latent array, never from a pool (sparse_mla)
+6. decode append: every request gains its newest token (append_tokens)
 
 Sources (web pages on latent-cache offload for DSA sparse decode):
 
@@ -37,6 +38,10 @@ Sources (web pages on latent-cache offload for DSA sparse decode):
   L_index*D_index)*P per token, the decode residency formula
   M_decode ~ L(C+2b)s_KV + ..., and the OverlapRatio definition in
   section "decode side (2)".
+* The same page, section "architecture: one master copy, two residency
+  policies" and its Figure 2: besides the hot cache of C slots the decode
+  side keeps two tail blocks that take the newly produced KV, and the host
+  keeps the authoritative copy paged by token block.
 * "ESS: Latent-Cache Offload" (foosynaptic tech notes): the indexer keeps
   one light vector per position and scores all positions to choose the
   top-2048; the latent entry is c^KV[512] + k^R[64]; the GPU sparse pool
@@ -49,7 +54,10 @@ go to the lower token index; the LRU recency unit is a per-layer step
 counter, hits are stamped before victims are chosen, and victims are
 ordered by (last_used asc, slot asc) with empty slots (last_used = -1)
 first; the i-th miss (ascending token) takes the i-th victim; the pool
-starts empty; attention outputs are float32.
+starts empty; attention outputs are float32; a newly appended token is
+not in the hot cache (it sits in a tail block), so it starts with
+cache_slots = -1 and is loaded into a slot, like any miss, when a step first
+selects it.
 
 Parity pins live in tests/test_oracle_pins.py.  Every function here is
 pinned by at least one value or property fixed by the pages or by
@@ -221,6 +229,24 @@ def lru_update(state: CacheState, union: np.ndarray, miss_tok: np.ndarray
 
 
 # --------------------------------------------------------------------------
+# 6. decode append
+# --------------------------------------------------------------------------
+
+def append_tokens(T: List[int], states: List[CacheState]) -> None:
+    """Every request gains its newest token: T_b grows by one and the new
+    token is not resident in the hot cache.
+
+    New KV goes to the tail blocks beside the hot cache, not into one of its
+    C slots, so cache_slots gets a -1 entry.  Whether the bytes sit in a tail
+    block or already in the host copy changes no result, so nothing about
+    them is tracked here.  Mutates T and states.
+    """
+    for b in range(len(T)):
+        T[b] += 1
+        states[b].cache_slots = np.append(states[b].cache_slots, np.int32(-1))
+
+
+# --------------------------------------------------------------------------
 # 5. sparse absorbed-MLA attention
 # --------------------------------------------------------------------------
 
@@ -273,6 +299,10 @@ class OracleLayer:
         self.sm_scale = float(sm_scale)
         self.page = page
         self.state = [CacheState.empty(t, C) for t in self.T]
+
+    def append(self) -> None:
+        """Decode append of one token per request (before the step that sees it)."""
+        append_tokens(self.T, self.state)
 
     def step(self, q_idx: np.ndarray, w: np.ndarray, keys: np.ndarray, scale: np.ndarray,
              q_mla: Optional[np.ndarray], latent: Optional[np.ndarray],

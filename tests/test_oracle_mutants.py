@@ -162,6 +162,19 @@ def mla_values_include_rope(q, rows, sm_scale, latent_dim=512):
     return (p @ shifted[:, :latent_dim]).astype(np.float32)
 
 
+# ------------------------------------------------------------------ append
+
+def append_without_growth(T, states):
+    pass
+
+
+def append_new_token_resident(T, states):
+    # the new token claims slot 0 as if it were already in the hot cache
+    for b in range(len(T)):
+        T[b] += 1
+        states[b].cache_slots = np.append(states[b].cache_slots, np.int32(0))
+
+
 MUTANTS = [
     ("score_indexer", score_no_relu),
     ("score_indexer", score_no_scale),
@@ -178,6 +191,8 @@ MUTANTS = [
     ("sparse_mla", mla_latent_only_logits),
     ("sparse_mla", mla_no_scale),
     ("sparse_mla", mla_values_include_rope),
+    ("append_tokens", append_without_growth),
+    ("append_tokens", append_new_token_resident),
 ]
 
 

@@ -445,3 +445,59 @@ def test_mla_large_logits_closed_form():
     got = O.sparse_mla(q, rows, 1.0)
     a = 1.0 / (1.0 + np.exp(-1.0))
     np.testing.assert_allclose(got[0], np.full(512, 3.0 * a - (1.0 - a)), rtol=1e-7)
+
+
+# --------------------------------------------------------------------------
+# decode append (FlashOffloading page, section "architecture" and Figure 2:
+# new KV goes to tail blocks beside the hot cache)
+# --------------------------------------------------------------------------
+
+def _append_run(T0, C, k, grow, seed):
+    """A one-request bf16 layer that appends a token before each of `grow`
+    steps; returns the layer data, the keys and latent of every token, the
+    oracle layer and each step's (result, q_mla)."""
+    cfg = W.tiny().replace(T=T0, k=k, C=C, grow=grow, seed=seed)
+    ld = W.gen_layer(cfg)
+    keys = W.decode_keys(cfg, ld.idx_keys)
+    keys[:, T0:T0 + grow] = W.decode_keys(cfg, ld.app_keys)
+    scale = ld.idx_scale.copy()
+    scale[:, T0:T0 + grow] = ld.app_scale
+    lat = W.bf16_bits_to_float(ld.latent).astype(np.float64)
+    lay = O.OracleLayer(ld.T, C, k, cfg.sm_scale)
+    qs = W.QueryStream(cfg)
+    res = []
+    for _ in range(grow):
+        lay.append()
+        q, _, qm = qs.next()
+        r = lay.step(q, W.head_weights(cfg, ld.w), keys, scale,
+                     W.bf16_bits_to_float(qm).astype(np.float64), lat)
+        res.append((r, W.bf16_bits_to_float(qm).astype(np.float64)))
+    return cfg, ld, lat, lay, res
+
+
+def test_append_every_token_attended_when_k_covers_the_context():
+    # k >= T: each step selects every token, the newest included, and the
+    # output is dense softmax attention over all of them; the newest token
+    # is the one miss of its step (it is not in the hot cache yet)
+    T0, grow = 60, 12
+    cfg, ld, lat, lay, res = _append_run(T0, C=256, k=256, grow=grow, seed=31)
+    for i, (r, qm) in enumerate(res):
+        T = T0 + 1 + i
+        assert sorted(r.topk[0][0].tolist()) == list(range(T))
+        want = scipy.special.softmax(cfg.sm_scale * qm[0, 0] @ lat[0, :T].T, axis=1) @ lat[0, :T, :512]
+        np.testing.assert_allclose(r.out[0, 0], want, rtol=1e-6, atol=1e-7)
+        if i > 0:
+            assert r.misses[0, 0] == 1 and r.miss_tok[0].tolist() == [T - 1]
+    assert lay.T == [T0 + grow]
+    assert lay.state[0].cache_slots.shape == (T0 + grow,)
+
+
+def test_append_keeps_the_cache_maps_consistent():
+    # a small pool under appends: cache_slots and slot_token stay inverse
+    # maps, the pool stays full once filled, and a selected token is resident
+    _, _, _, lay, res = _append_run(500, C=96, k=64, grow=40, seed=32)
+    st = lay.state[0]
+    _check_bijection(st)
+    assert np.all(st.cache_slots[res[-1][0].topk[0][0]] >= 0)
+    assert np.count_nonzero(st.slot_token >= 0) == 96
+    assert sum(int(r.miss_tok[0].shape[0]) for r, _ in res) >= 96
