@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--pipeline", type=int, default=0,
                     help="time L layers of the workload as two micro-batches (half the "
                          "requests each) on two streams against the same work on one stream")
+    ap.add_argument("--append", action="store_true",
+                    help="time decode steps that each append one token per request first")
     ap.add_argument("--miss-sweep", default=None,
                     help="comma-separated hot-pool sizes C: print the distinct miss rows per "
                          "step of the workload for each instead of the benchmark line")
@@ -356,17 +358,23 @@ def measure_overlap(cfg, ld, n_steps, stream, host_buffers):
                                                   outs[ess.ESS_MISS_STAGED]))}
 
 
-# sources of the indexer kernel; the DRAM traffic taken by ncu holds only
-# while they are unchanged
-INDEXER_SOURCES = ("ess_indexer.cu", "ess_device.cuh", "ess_internal.h")
+# what the indexer kernel's device code is built from: its own file, the
+# device helpers, and the compile-time constants of the shared header (the
+# rest of that header declares host-side state); the DRAM traffic taken by
+# ncu holds only while these are unchanged
+INDEXER_SOURCES = ("ess_indexer.cu", "ess_device.cuh")
+INDEXER_CONSTANTS = "ess_internal.h"
 
 
 def indexer_source_digest() -> str:
     import hashlib
     h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "host_latent_cache_gb300", "csrc")
     for name in INDEXER_SOURCES:
-        with open(os.path.join(ROOT, "host_latent_cache_gb300", "csrc", name), "rb") as f:
+        with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
+    with open(os.path.join(csrc, INDEXER_CONSTANTS), "rb") as f:
+        h.update(b"".join(l for l in f.read().splitlines(True) if b"constexpr" in l))
     return h.hexdigest()[:16]
 
 
@@ -677,6 +685,73 @@ def pipeline_bench(args, cfg):
     return 0
 
 
+def append_bench(args, cfg):
+    """Decode with appends: a step that first appends one token per request
+    (ess_append: the ring row, the indexer key, a completed page back to host
+    memory), then runs the layer over the grown context.  After warm-up steps
+    that fill the pool, blocks of steps with and without appends alternate
+    (twice each) on the same pool, timed with CUDA events; then the append
+    kernel alone, back to back."""
+    import torch
+    from host_latent_cache_gb300 import ess
+    from host_latent_cache_gb300.session import Session
+    ess.load()
+    K = args.steps
+    n_app = 3 * K
+    c = cfg.replace(grow=n_app)
+    ld = W.gen_layer(c)
+    sess = Session(c, [ld])
+    qs = W.QueryStream(c)
+    wts = W.head_weights(c, ld.w)
+    ins = []
+    for _ in range(args.warmup + 4 * K):
+        _, enc, qm = qs.next()
+        ins.append(sess.device_inputs(enc, wts, qm))
+    apps = [sess.append_inputs(*W.appended_token(c, ld, i)) for i in range(n_app)]
+    del ld
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nq = na = 0
+
+    def block(n, append, step):
+        nonlocal nq, na
+        torch.cuda.synchronize()
+        e0.record(st)
+        for _ in range(n):
+            if append:
+                ess.ess_append(sess.pool, 0, *apps[na], st)
+                na += 1
+            if step:
+                qd, wd, qmd = ins[nq]
+                nq += 1
+                ess.ess_step(sess.pool, 0, qd, wd, qmd, sess.out, st)
+        e1.record(st)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    block(args.warmup, False, True)
+    runs = {"with_append": [], "without_append": []}
+    for _ in range(2):
+        runs["with_append"].append(block(K, True, True))
+        runs["without_append"].append(block(K, False, True))
+    alone = block(K, True, False)
+    assert sess.poll(st) == ess.ESS_OK
+    sess.close()
+    units = cfg.batch * cfg.mtp
+    mean = {m: sum(v) / len(v) for m, v in runs.items()}
+    line = {"append": {"workload": cfg.name, "steps_per_block": K, "warmup": args.warmup,
+                       "T_start": cfg.T, "tokens_appended_per_request": na,
+                       "timing": "CUDA events on the launching stream around each block",
+                       "with_append_us_per_step": runs["with_append"],
+                       "without_append_us_per_step": runs["without_append"],
+                       "append_kernel_alone_us": alone,
+                       "with_append_token_layers_per_s": units / (mean["with_append"] * 1e-6),
+                       "without_append_token_layers_per_s":
+                           units / (mean["without_append"] * 1e-6)}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
@@ -685,6 +760,8 @@ def main():
         return miss_sweep(args, cfg) if rank == 0 else 0
     if args.pipeline:
         return pipeline_bench(args, cfg) if rank == 0 else 0
+    if args.append:
+        return append_bench(args, cfg) if rank == 0 else 0
     if args.impl == "reference":
         return bench_reference(args, cfg, rank, world)
     result, ld = bench_ours(args, cfg, rank, world, local_rank)

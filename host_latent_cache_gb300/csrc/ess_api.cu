@@ -56,6 +56,8 @@ Layout compute_layout(const ess_config& c) {
   L.o_lused = o;    o = align256(o + B * C * 4);
   L.o_order = o;    o = align256(o + 2 * B * C * 4);
   L.o_pool = o;     o = align256(o + B * C * kRowBytes);
+  L.o_T0 = o;       o = align256(o + B * 4);
+  L.o_tail = o;     o = align256(o + B * 2 * c.page * kRowBytes);
   L.layer_bytes = o;
   o = L.layer_bytes * c.n_layers;
   L.o_scores = o;   o = align256(o + B * M * T * 4);
@@ -224,6 +226,8 @@ ess_status ess_pool_create(const ess_config* cfg, void* dev_workspace, size_t ws
     y.last_used = reinterpret_cast<int32_t*>(base + L.o_lused);
     y.order = reinterpret_cast<int32_t*>(base + L.o_order);
     y.pool = reinterpret_cast<uint16_t*>(base + L.o_pool);
+    y.T0_dev = reinterpret_cast<int32_t*>(base + L.o_T0);
+    y.tail = reinterpret_cast<uint16_t*>(base + L.o_tail);
   }
   Scratch& r = p->scr;
   r.scores = reinterpret_cast<float*>(p->ws + L.o_scores);
@@ -290,8 +294,11 @@ ess_status ess_pool_bind_layer(ess_pool* pool, int layer, const void* host_laten
                      static_cast<uint64_t>(c.batch) * c.max_T, kKeyRowBytes, kKeyRowBytes, kIdxTile))
     return ESS_ERR_CUDA;
   if (cudaMemcpy(L.T_dev, T_host, c.batch * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(L.T0_dev, T_host, c.batch * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemcpy(L.tile_off, tiles.data(), (c.batch + 1) * 4, cudaMemcpyHostToDevice) != cudaSuccess)
     return ESS_ERR_CUDA;
+  L.T0_host.assign(T_host, T_host + c.batch);
+  L.n_appended = 0;
   L.host_latent = static_cast<const uint16_t*>(dev_alias);
   L.page_table = page_table;
   L.idx_keys = static_cast<const uint8_t*>(idx_keys);
@@ -305,6 +312,33 @@ ess_status ess_pool_bind_layer(ess_pool* pool, int layer, const void* host_laten
 ess_status ess_pool_reset(ess_pool* pool, int layer, ess_stream_t stream) {
   if (!pool || layer < 0 || layer >= pool->cfg.n_layers) return ESS_ERR_INVALID_ARG;
   return cuda_status(launch_reset(*pool, layer, static_cast<cudaStream_t>(stream)));
+}
+
+ess_status ess_append(ess_pool* pool, int layer, const void* latent_row, const void* key_row,
+                      const float* key_scale, ess_stream_t stream) {
+  if (!pool || layer < 0 || layer >= pool->cfg.n_layers || !latent_row || !key_row)
+    return ESS_ERR_INVALID_ARG;
+  const ess_config& c = pool->cfg;
+  Layer& L = pool->layers[layer];
+  if (!L.bound || !aligned16(latent_row) || !aligned16(key_row)) return ESS_ERR_INVALID_ARG;
+  if (L.idx_scale && !key_scale) return ESS_ERR_INVALID_ARG;
+  const int n = L.n_appended + 1;   // tokens appended after this call
+  for (int b = 0; b < c.batch; ++b)
+    if (L.T0_host[b] + n > c.max_T) return ESS_ERR_CAPACITY;
+  const cudaError_t e = launch_append(*pool, layer, latent_row, key_row, key_scale,
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return ESS_ERR_CUDA;
+  // the host copies of T_b that size the indexer and selection launches
+  int tiles = 0, tmax = 0;
+  for (int b = 0; b < c.batch; ++b) {
+    const int T = L.T0_host[b] + n;
+    tiles += (T + kIdxTile - 1) / kIdxTile;
+    tmax = T > tmax ? T : tmax;
+  }
+  L.n_appended = n;
+  L.total_tiles = tiles;
+  L.T_hmax = tmax;
+  return ESS_OK;
 }
 
 ess_status ess_indexer_scores(ess_pool* pool, int layer, const void* q_idx, const float* w,

@@ -1,0 +1,134 @@
+// Decode append: the newest token of every request joins the layer.
+//
+// hwcomputing.csdn.net FlashOffloading analysis, section "architecture: one
+// master copy, two residency policies" and its Figure 2: on the decode side
+// the device keeps the model's own indexer state, the hot cache of C slots,
+// the cache_slots table and two tail blocks that take the newly produced KV;
+// the authoritative KV lives in host memory, paged by (request, layer, token
+// block) behind a block table.
+//
+// The page names the parts but not the steps; the reading taken here:
+//   - token t of request b is written to row t mod (2 * page) of the
+//     request's two-page device ring, and its indexer key (and scale) to row
+//     t of the layer's indexer cache, so the next indexer pass scores it;
+//   - when t completes a page, the appended rows of that page are written
+//     back to their host rows through the block table;
+//   - a ring row is overwritten by token t + 2 * page, so rows of the newest
+//     two pages (tokens >= page * floor(T_b / page) - page) are read from the
+//     ring and older ones from the host copy;
+//   - cache_slots stays -1 for a new token: it is not in the hot cache, and a
+//     step that selects it loads it into a slot like any other miss (from the
+//     ring while it is there).
+#include "ess_device.cuh"
+
+namespace ess {
+namespace {
+
+struct AppendArgs {
+  const uint16_t* latent;     // [B][D] bf16: the new rows
+  const uint8_t* key;         // [B][128 bytes]: the new indexer key rows
+  const float* key_scale;     // [B], used when the layer has per-token scales
+  uint8_t* idx_keys;          // [B][T][128 bytes]
+  float* idx_scale;           // [B][T] or null
+  uint16_t* tail;             // [B][2 * page][D]
+  uint16_t* host;             // [B][T][D] device alias of the pinned host rows
+  const int32_t* page_table;  // [B][T / page] or null
+  int32_t* Tb;                // [B]
+  const int32_t* T0;          // [B] T_b at the bind
+  int32_t* tile_off;          // [B+1] prefix of indexer tiles
+  int* status;
+  int T, page, npages;
+  int n_before;               // tokens appended to every request before this call
+};
+
+constexpr int kAppendThreads = 256;
+constexpr int kRowVec = kRowBytes / 16;      // 72 16-byte units per latent row
+constexpr int kKeyVec = kKeyRowBytes / 16;   // 8 per key row
+
+// One CTA per request.  Launched as a programmatic dependent but without a
+// trigger of its own: the next kernels (the indexer, or an attention kernel
+// that reads T_b before it waits) start only after this grid has finished.
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs a) {
+  pdl_wait_previous();   // the previous step still reads T_b, the ring and the keys
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int t = a.T0[b] + a.n_before;
+  const bool bad = t < 0 || t >= a.T || a.Tb[b] != t;
+  __syncthreads();       // every thread has read T_b before it changes below
+  if (bad) {
+    if (tid == 0) set_status(a.status, ESS_ERR_DEVICE_CHECK);
+    return;
+  }
+  const int ring = 2 * a.page;
+  uint16_t* trow = a.tail + (static_cast<size_t>(b) * ring + t % ring) * kRowDim;
+  if (tid < kRowVec) {
+    reinterpret_cast<uint4*>(trow)[tid] =
+        reinterpret_cast<const uint4*>(a.latent + static_cast<size_t>(b) * kRowDim)[tid];
+  } else if (tid >= 128 && tid < 128 + kKeyVec) {
+    const int q = tid - 128;
+    reinterpret_cast<uint4*>(a.idx_keys + (static_cast<size_t>(b) * a.T + t) * kKeyRowBytes)[q] =
+        reinterpret_cast<const uint4*>(a.key + static_cast<size_t>(b) * kKeyRowBytes)[q];
+  } else if (tid == 160) {
+    if (a.idx_scale) a.idx_scale[static_cast<size_t>(b) * a.T + t] = a.key_scale[b];
+  } else if (tid == 192) {
+    // T_b and this request's end of the tile prefix; every request grows by
+    // one token, so the prefix follows from the bind-time lengths
+    a.Tb[b] = t + 1;
+    int tiles = 0;
+    for (int i = 0; i <= b; ++i) tiles += (a.T0[i] + a.n_before + 1 + kIdxTile - 1) / kIdxTile;
+    a.tile_off[b + 1] = tiles;
+  }
+  if ((t + 1) % a.page != 0) return;
+
+  // t completes its page: copy the page's appended rows to the host copy
+  __syncthreads();       // the new row is in the ring
+  const int pg = t / a.page;
+  int hrow0 = pg * a.page;
+  if (a.page_table) {
+    const int pp = a.page_table[static_cast<size_t>(b) * a.npages + pg];
+    if (pp < 0 || pp >= a.npages) {
+      if (tid == 0) set_status(a.status, ESS_ERR_DEVICE_CHECK);
+      return;
+    }
+    hrow0 = pp * a.page;
+  }
+  const int first = a.T0[b] > pg * a.page ? a.T0[b] : pg * a.page;   // first appended token
+  const int n = (t + 1 - first) * kRowVec;
+  for (int i = tid; i < n; i += kAppendThreads) {
+    const int tok = first + i / kRowVec, q = i % kRowVec;
+    const uint4 v =
+        reinterpret_cast<const uint4*>(a.tail + (static_cast<size_t>(b) * ring + tok % ring) * kRowDim)[q];
+    reinterpret_cast<uint4*>(a.host + (static_cast<size_t>(b) * a.T + hrow0 + tok % a.page) * kRowDim)[q] = v;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const ess_pool& p, int layer, const void* latent, const void* key,
+                          const float* key_scale, cudaStream_t st) {
+  const ess_config& c = p.cfg;
+  const Layer& L = p.layers[layer];
+  AppendArgs a;
+  a.latent = static_cast<const uint16_t*>(latent);
+  a.key = static_cast<const uint8_t*>(key);
+  a.key_scale = key_scale;
+  // the caller's indexer cache and host copy grow with the context: the
+  // binding hands them over for these writes
+  a.idx_keys = const_cast<uint8_t*>(L.idx_keys);
+  a.idx_scale = const_cast<float*>(L.idx_scale);
+  a.tail = L.tail;
+  a.host = const_cast<uint16_t*>(L.host_latent);
+  a.page_table = L.page_table;
+  a.Tb = L.T_dev;
+  a.T0 = L.T0_dev;
+  a.tile_off = L.tile_off;
+  a.status = p.scr.status;
+  a.T = c.max_T;
+  a.page = c.page;
+  a.npages = c.max_T / c.page;
+  a.n_before = L.n_appended;
+  const cudaError_t e = launch_pdl(append_kernel, dim3(c.batch), dim3(kAppendThreads), 0, st, a);
+  if (e == cudaSuccess) count_launch(p);
+  return e;
+}
+
+}  // namespace ess

@@ -13,7 +13,8 @@
 // One CTA handles 128 selected rows of one (request, way), assigned with a
 // stride over the emitted list so the misses at its head spread over all
 // CTAs.  Rows are gathered with 16-byte cp.async straight from the pool
-// (HBM) or from pinned host memory (UVA) into 128B-swizzled shared memory;
+// (HBM) or from pinned host memory (UVA) into 128B-swizzled shared memory
+// (a miss among the newest appended tokens comes from their device ring);
 // tcgen05.mma computes S[128 heads][128 rows] = Q * R^T (bf16, fp32 in
 // TMEM) one 64-dim block at a time as rows land; the softmax numerator P is
 // formed in fp32 and split into two bf16 terms P = P_hi + P_lo (about 16
@@ -44,6 +45,8 @@ struct AttnArgs {
   const int32_t* page_table;  // [B][T/page] or null
   uint16_t* pool;             // [B][C][576]
   const uint16_t* host;       // [B][T][576] (device alias of pinned host memory)
+  const uint16_t* tail;       // [B][2*page][576] ring of the newest appended rows
+  const int32_t* T0;          // [B] tokens >= T0_b were appended after the bind
   uint16_t* part_o;           // [B][M][nch][H][512] fp16 (unit u of head h at u ^ (h & 7))
   float2* part_ml;            // [B][M][nch][H]
   int* status;
@@ -78,6 +81,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int c = blockIdx.x, m = blockIdx.y, b = blockIdx.z;
   const int Tb = a.Tb[b];
   const int nsel = a.k < Tb ? a.k : Tb;
+  // appended tokens of the two newest pages are read from the device ring
+  const int tail_lo = max(a.T0[b], (Tb / a.page - 1) * a.page);
   // rows j = 0..cnt-1 hold entries c + j * nch of the emitted list
   int cnt = 0;
   if (c < nsel) cnt = (nsel - 1 - c) / a.nch + 1;
@@ -141,7 +146,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       set_status(a.status, ESS_ERR_DEVICE_CHECK);
       valid = false;
     } else if (miss && !a.staged) {
-      src = a.host + (static_cast<size_t>(b) * a.T + prow) * kRowDim;
+      src = t >= tail_lo
+                ? a.tail + (static_cast<size_t>(b) * 2 * a.page + t % (2 * a.page)) * kRowDim
+                : a.host + (static_cast<size_t>(b) * a.T + prow) * kRowDim;
     } else {
       src = a.pool + (static_cast<size_t>(b) * a.C + slot) * kRowDim;
     }
@@ -404,13 +411,15 @@ __global__ void __launch_bounds__(128) merge_kernel(const uint16_t* __restrict__
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
-// (a6) one warp per miss row: host row of miss_tok -> pool slot miss_slot
+// (a6) one warp per miss row: host (or ring) row of miss_tok -> pool slot miss_slot
 __global__ void __launch_bounds__(256) stage_kernel(const int32_t* __restrict__ miss_tok,
                                                     const int32_t* __restrict__ miss_slot,
                                                     const int32_t* __restrict__ n_miss,
                                                     const int32_t* __restrict__ Tb,
                                                     const int32_t* __restrict__ page_table,
                                                     const uint16_t* __restrict__ host,
+                                                    const uint16_t* __restrict__ tail,
+                                                    const int32_t* __restrict__ T0,
                                                     uint16_t* __restrict__ pool, int MK, int C,
                                                     int T, int page, int npages, int* status) {
   pdl_wait_previous();
@@ -428,7 +437,11 @@ __global__ void __launch_bounds__(256) stage_kernel(const int32_t* __restrict__ 
     if (lane == 0) set_status(status, ESS_ERR_DEVICE_CHECK);
     return;
   }
-  const uint4* s = reinterpret_cast<const uint4*>(host + (static_cast<size_t>(b) * T + prow) * kRowDim);
+  // appended tokens of the two newest pages come from the device ring
+  const int tail_lo = max(T0[b], (Tb[b] / page - 1) * page);
+  const uint4* s = reinterpret_cast<const uint4*>(
+      t >= tail_lo ? tail + (static_cast<size_t>(b) * 2 * page + t % (2 * page)) * kRowDim
+                   : host + (static_cast<size_t>(b) * T + prow) * kRowDim);
   uint4* d = reinterpret_cast<uint4*>(pool + (static_cast<size_t>(b) * C + v) * kRowDim);
   uint4 r[3];
 #pragma unroll
@@ -459,6 +472,8 @@ cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
   a.page_table = L.page_table;
   a.pool = L.pool;
   a.host = L.host_latent;
+  a.tail = L.tail;
+  a.T0 = L.T0_dev;
   a.part_o = p.scr.part_o;
   a.part_ml = p.scr.part_ml;
   a.status = p.scr.status;
@@ -498,7 +513,9 @@ cudaError_t launch_stage(const ess_pool& p, int layer, const int32_t* miss_tok,
   const cudaError_t e =
       launch_pdl(stage_kernel, grid, dim3(256), 0, st, miss_tok, miss_slot, n_miss,
                  static_cast<const int32_t*>(L.T_dev), static_cast<const int32_t*>(L.page_table),
-                 L.host_latent, L.pool, MK, c.C, c.max_T, c.page, c.max_T / c.page, p.scr.status);
+                 L.host_latent, static_cast<const uint16_t*>(L.tail),
+                 static_cast<const int32_t*>(L.T0_dev), L.pool, MK, c.C, c.max_T, c.page,
+                 c.max_T / c.page, p.scr.status);
   if (e == cudaSuccess) count_launch(p);
   return e;
 }

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "ess.h"
 
 namespace ess {
@@ -43,6 +45,12 @@ struct Layer {
   int32_t* tile_off = nullptr;    // [B+1] prefix of indexer tiles
   int32_t total_tiles = 0;
   int32_t T_hmax = 0;             // max over requests of T_b
+  // decode append: tokens t >= T0_b were appended after the bind; the two
+  // newest pages of them sit in a device ring until the host copy takes over
+  int32_t* T0_dev = nullptr;      // [B] T_b at the bind
+  uint16_t* tail = nullptr;       // [B][2 * page][D] bf16, token t at row t % (2 * page)
+  std::vector<int32_t> T0_host;   // host copy of T0_dev
+  int32_t n_appended = 0;         // tokens appended to every request since the bind
   CUtensorMap kmap;               // keys as [B*T rows][128 B], 128x128 boxes, 128B swizzle
   // state
   int32_t* cache_slots = nullptr; // [B][T]
@@ -78,7 +86,8 @@ struct Layout {
   size_t total = 0;
   size_t layer_bytes = 0;
   // per layer (relative to the layer base)
-  size_t o_T, o_tiles, o_cslots, o_stoken, o_lused, o_step, o_pool, o_stats, o_order;
+  size_t o_T, o_tiles, o_cslots, o_stoken, o_lused, o_step, o_pool, o_stats, o_order, o_T0,
+      o_tail;
   // scratch (absolute)
   size_t o_scores, o_tidx, o_tslot, o_nmw, o_mtok, o_mslot, o_nmiss, o_vict, o_hist, o_po, o_pml,
       o_hq, o_hw, o_hqm, o_hout, o_status;
@@ -159,6 +168,8 @@ cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
                              const int32_t* topk_idx, const int32_t* topk_slot, float* out,
                              bool misses_staged, bool early, cudaStream_t st);
 cudaError_t launch_reset(const ess_pool& p, int layer, cudaStream_t st);
+cudaError_t launch_append(const ess_pool& p, int layer, const void* latent, const void* key,
+                          const float* key_scale, cudaStream_t st);
 
 // Encodes a 2-D tiled tensor map; returns false on failure.
 bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,

@@ -32,7 +32,8 @@ ESS_MISS_STAGED = 1
 EXPORTS = (
     "ess_status_string", "ess_host_alloc", "ess_host_free", "ess_pool_device_bytes",
     "ess_pool_create", "ess_pool_destroy",
-    "ess_pool_bind_layer", "ess_pool_reset", "ess_indexer_scores", "ess_select_manage",
+    "ess_pool_bind_layer", "ess_pool_reset", "ess_append", "ess_indexer_scores",
+    "ess_select_manage",
     "ess_select_manage_noalloc",
     "ess_indexer_topk", "ess_stage_misses", "ess_sparse_mla_decode", "ess_step",
     "ess_step_profiled", "ess_step_host",
@@ -87,6 +88,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "ess_pool_destroy": [P],
         "ess_pool_bind_layer": [P, I, P, P, P, P, P],
         "ess_pool_reset": [P, I, P],
+        "ess_append": [P, I, P, P, P, P],
         "ess_indexer_scores": [P, I, P, P, P, P],
         "ess_select_manage": [P, I, P, P, P, P, P, P, P, P],
         "ess_select_manage_noalloc": [P, I, P, P, P, P, P, P, P, P],
@@ -203,6 +205,11 @@ def ess_pool_bind_layer(pool, layer, host_latent, page_table, idx_keys, idx_scal
 
 def ess_pool_reset(pool, layer, stream=None) -> None:
     check(load().ess_pool_reset(pool, layer, _stream(stream)), "ess_pool_reset")
+
+
+def ess_append(pool, layer, latent_row, key_row, key_scale, stream=None) -> None:
+    check(load().ess_append(pool, layer, _p(latent_row), _p(key_row), _p(key_scale),
+                            _stream(stream)), "ess_append")
 
 
 def ess_indexer_scores(pool, layer, q_idx, w, scores, stream=None) -> None:

@@ -77,7 +77,17 @@ class Session:
         qm = torch.from_numpy(np.ascontiguousarray(q_mla).view(np.int16)).to(self.device)
         return q, wt, qm
 
+    def append_inputs(self, latent_rows: np.ndarray, key_rows: np.ndarray, scales: np.ndarray):
+        """Device copies of one decode append's inputs (see W.appended_token)."""
+        lat = torch.from_numpy(np.ascontiguousarray(latent_rows).view(np.int16)).to(self.device)
+        key = torch.from_numpy(np.ascontiguousarray(key_rows)).to(self.device)
+        sc = torch.from_numpy(np.ascontiguousarray(scales, dtype=np.float32)).to(self.device)
+        return lat, key, sc
+
     # -------------------------------------------------------------- calls
+    def append(self, layer, latent_rows, key_rows, scales, stream=None):
+        ess.ess_append(self.pool, layer, latent_rows, key_rows, scales, stream)
+
     def scores_only(self, layer, q, w, stream=None):
         ess.ess_indexer_scores(self.pool, layer, q, w, self.scores, stream)
         return self.scores

@@ -108,8 +108,8 @@ const char* ess_status_string(ess_status s);
 
 /* Bytes of device workspace that ess_pool_create needs for cfg.
  * Covers, per layer: cache_slots [B][T] int32, slot_token [B][C] int32,
- * last_used [B][C] int32, step [B] int32, the hot pool [B][C][D] bf16 and
- * counters; plus scratch shared by the layers (scores, selection lists,
+ * last_used [B][C] int32, step [B] int32, the hot pool [B][C][D] bf16, the
+ * ring of appended rows [B][2 * page][D] bf16 and counters; plus scratch shared by the layers (scores, selection lists,
  * attention partials, staging for ess_step_host).
  * Errors: ESS_ERR_INVALID_ARG / ESS_ERR_UNSUPPORTED for a bad cfg. */
 ess_status ess_pool_device_bytes(const ess_config* cfg, size_t* bytes);
@@ -144,13 +144,37 @@ ess_status ess_host_free(void* ptr);
  *                keys (d_I = 64)
  *   idx_scale    device float [B][T] per-token key scale, or NULL for 1.0
  *   T_host       host int32 [B], tokens per request, 0 <= T_b <= max_T
- * Buffers must stay valid and unchanged while the layer is used. */
+ * Buffers must stay valid while the layer is used.  The library changes them
+ * only through ess_append, which writes rows t >= T_b of idx_keys, idx_scale
+ * and (once a page of new tokens is complete) host_latent. */
 ess_status ess_pool_bind_layer(ess_pool* pool, int layer, const void* host_latent,
                                const int32_t* page_table, const void* idx_keys,
                                const float* idx_scale, const int32_t* T_host);
 
 /* Empty the hot pool of a layer again (asynchronous on stream). */
 ess_status ess_pool_reset(ess_pool* pool, int layer, ess_stream_t stream);
+
+/* Decode append: the newest token of every request joins the layer, so T_b
+ * grows by one for each b ([FO] "architecture" and its Figure 2: besides the
+ * hot cache the device keeps two tail blocks that take the new KV; the host
+ * keeps the authoritative copy, paged behind the block table).
+ *   latent_row  device bf16 [B][D], 16-byte aligned: the new token's c^KV|k^R
+ *   key_row     device [B][128 bytes], 16-byte aligned: its indexer key, in
+ *               the encoding of the bound idx_keys
+ *   key_scale   device float [B]: its key scale; required when the layer
+ *               was bound with idx_scale, ignored otherwise
+ * Token t = T_b is written to row t of idx_keys (and idx_scale) and to a
+ * device ring of two pages per request; when t completes a page, that page's
+ * appended rows are written to their host_latent rows through the page table.
+ * Until then (and for one more page) the gathers read them from the ring.  A
+ * new token is not in the hot pool (cache_slots stays -1): the first step
+ * that selects it loads it into a slot like any other miss.  Call it before
+ * the step that should see the token.  Asynchronous on stream (one kernel).
+ * Errors: ESS_ERR_CAPACITY, launching nothing, when a request is already at
+ * max_T; ESS_ERR_INVALID_ARG for an unbound layer, a null or misaligned
+ * row, or a missing key_scale. */
+ess_status ess_append(ess_pool* pool, int layer, const void* latent_row, const void* key_row,
+                      const float* key_scale, ess_stream_t stream);
 
 /* (a1) Indexer scores ([ESS]: score all positions; formula
  * S[b][m][t] = fl32(scale[b][t] * sum_h w[b][m][h] * ReLU(q[b][m][h] . k[b][t]))).
