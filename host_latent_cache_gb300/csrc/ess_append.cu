@@ -45,11 +45,13 @@ constexpr int kAppendThreads = 256;
 constexpr int kRowVec = kRowBytes / 16;      // 72 16-byte units per latent row
 constexpr int kKeyVec = kKeyRowBytes / 16;   // 8 per key row
 
-// One CTA per request.  Launched as a programmatic dependent but without a
-// trigger of its own: the next kernels (the indexer, or an attention kernel
-// that reads T_b before it waits) start only after this grid has finished.
+// One CTA per request, launched as a programmatic dependent.  Its own
+// dependents may start at once: every kernel of the library waits for this
+// grid to finish (griddepcontrol.wait) before it reads T_b, the keys or the
+// ring.
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendArgs a) {
   pdl_wait_previous();   // the previous step still reads T_b, the ring and the keys
+  pdl_launch_dependents();
   const int b = blockIdx.x, tid = threadIdx.x;
   const int t = a.T0[b] + a.n_before;
   const bool bad = t < 0 || t >= a.T || a.Tb[b] != t;

@@ -79,14 +79,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int c = blockIdx.x, m = blockIdx.y, b = blockIdx.z;
-  const int Tb = a.Tb[b];
-  const int nsel = a.k < Tb ? a.k : Tb;
-  // appended tokens of the two newest pages are read from the device ring
-  const int tail_lo = max(a.T0[b], (Tb / a.page - 1) * a.page);
-  // rows j = 0..cnt-1 hold entries c + j * nch of the emitted list
-  int cnt = 0;
-  if (c < nsel) cnt = (nsel - 1 - c) / a.nch + 1;
-  if (cnt > NCH_ROWS) cnt = NCH_ROWS;
   const size_t wo = (static_cast<size_t>(b) * a.M + m) * a.k;
   const int qrow0 = (b * a.M + m) * a.H;
 
@@ -109,8 +101,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // everything above touched only this CTA's shared memory and TMEM
+  // everything above touched only this CTA's shared memory and TMEM.  Early:
+  // T_b was final before the selection ahead of this grid could launch.
   if (!a.early) pdl_wait_previous();
+  const int Tb = a.Tb[b];
+  const int nsel = a.k < Tb ? a.k : Tb;
+  // appended tokens of the two newest pages are read from the device ring
+  const int tail_lo = max(a.T0[b], (Tb / a.page - 1) * a.page);
+  // rows j = 0..cnt-1 hold entries c + j * nch of the emitted list
+  int cnt = 0;
+  if (c < nsel) cnt = (nsel - 1 - c) / a.nch + 1;
+  if (cnt > NCH_ROWS) cnt = NCH_ROWS;
 
   // query blocks 0..3 into the stage ring
   if (tid == 32) {
