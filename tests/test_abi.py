@@ -52,7 +52,8 @@ def test_device_bytes_matches_layout(lib):
     B_, T, C, M, k, H = 8, 131072, 32768, 1, 2048, 128
     state = B_ * T * 4 + 2 * B_ * C * 4 + B_ * C * 1152
     partials = B_ * M * (k // 128) * H * 512 * 2      # fp16 chunk partials
-    assert state + partials < n < state + partials + 64 * 2 ** 20
+    ring = B_ * 2 * 64 * 1152                         # appended rows: two pages per request
+    assert state + partials + ring < n < state + partials + ring + 64 * 2 ** 20
 
 
 @pytest.mark.parametrize("field,value,code", [
@@ -80,6 +81,7 @@ def test_create_rejects_bad_workspace_without_touching_a_gpu(lib):
                                ctypes.byref(h)) == ess.ESS_ERR_INVALID_ARG
     assert lib.ess_pool_destroy(None) == ess.ESS_ERR_INVALID_ARG
     assert lib.ess_step(None, 0, None, None, None, None, None) == ess.ESS_ERR_INVALID_ARG
+    assert lib.ess_append(None, 0, None, None, None, None) == ess.ESS_ERR_INVALID_ARG
 
 
 def test_missing_library_fails_loudly(tmp_path):
