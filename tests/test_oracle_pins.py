@@ -501,3 +501,25 @@ def test_append_keeps_the_cache_maps_consistent():
     assert np.all(st.cache_slots[res[-1][0].topk[0][0]] >= 0)
     assert np.count_nonzero(st.slot_token >= 0) == 96
     assert sum(int(r.miss_tok[0].shape[0]) for r, _ in res) >= 96
+
+
+def test_generator_append_inputs_continue_the_same_streams():
+    # the rows a decode append feeds in are the rows a longer context would
+    # have had: keys, scales and latent come from the same seeded streams,
+    # and the bound cache and host copy start empty past T_b
+    cfg = W.long_128k().replace(batch=2, T=300, T_per_req=[300, 170], grow=40)
+    ld = W.gen_layer(cfg)
+    full = W.gen_layer(cfg.replace(T_per_req=[340, 210], grow=0))
+    assert W.t_max_of(cfg) == W.t_max_of(cfg.replace(T_per_req=[340, 210], grow=0)) == 384
+    for b, T in enumerate([300, 170]):
+        assert np.array_equal(ld.app_keys[b], full.idx_keys[b, T:T + 40])
+        assert np.array_equal(ld.app_scale[b], full.idx_scale[b, T:T + 40])
+        assert np.all(ld.idx_keys[b, T:] == 0) and np.all(ld.idx_scale[b, T:] == 1.0)
+        assert np.array_equal(ld.latent[b], full.latent[b])
+        t = np.arange(W.t_max_of(cfg))
+        phys = ld.page_table[b][t // cfg.page] * cfg.page + t % cfg.page
+        assert np.array_equal(ld.host_latent[b][phys[:T]], ld.latent[b, :T])
+        assert np.all(ld.host_latent[b][phys[T:]] == 0)
+        lat, key, sc = W.appended_token(cfg, ld, 7)
+        assert np.array_equal(lat[b], full.latent[b, T + 7]) and np.array_equal(key[b], full.idx_keys[b, T + 7])
+        assert sc[b] == full.idx_scale[b, T + 7]
