@@ -34,6 +34,11 @@
 // |Miss| of them are the victims, already in the order that pairs the i-th
 // miss with the i-th victim; the next list is the remaining unstamped
 // entries followed by the stamped slots in slot order.
+//
+// Two kernels share this work: select_kernel produces everything the step
+// reads (the emitted lists, the miss union and its victims), and
+// lru_finish_kernel, which only the next step depends on, rewrites the state
+// and closes the next LRU list while the attention kernel runs.
 #include <mutex>
 
 #include "ess_device.cuh"
