@@ -10,7 +10,9 @@
  *   victim choice and state rewrite with copy triples, (a5) sparse
  *   absorbed-MLA attention whose row gather forks per row: hits from the
  *   HBM hot pool, misses straight from pinned host memory, (a6) a separate
- *   miss-staging copy, and per-step counters.
+ *   miss-staging copy, per-step counters, and the decode append of each
+ *   step's new token (a device ring of two pages, written back to the host
+ *   copy a page at a time).
  *
  * Sources (web pages on latent-cache offload for DSA sparse decode):
  *   [FO]  hwcomputing.csdn.net, analysis of FlashOffloading
@@ -18,7 +20,8 @@
  *           the MTP3 miss union, LIM and its worked example (Figure 4);
  *         - "decode side (2)": CopySFA, the gather that forks on hit/miss;
  *         - "architecture": one host master copy, paged by request, layer
- *           and token block behind a block table; a hot cache of C slots.
+ *           and token block behind a block table; a hot cache of C slots
+ *           and two tail blocks for the new KV (Figure 2).
  *   [ESS] foosynaptic tech notes, "ESS: Latent-Cache Offload": the indexer
  *         cache stays on the GPU and scores every position; the latent
  *         entry is c^KV[512] + k^R[64]; a GPU sparse pool under LRU.
