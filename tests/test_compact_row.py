@@ -181,7 +181,7 @@ def test_pins_catch_mutant(monkeypatch, name, mutant):
     for pin in PINS:
         try:
             pin()
-        except Exception as e:
+        except (Exception, pytest.fail.Exception) as e:   # an assertion or a pytest.raises miss
             failed.append(f"{pin.__name__}: {type(e).__name__}")
             break
     assert failed, f"no pin notices {mutant.__name__}"
