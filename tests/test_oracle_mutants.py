@@ -202,7 +202,8 @@ def _pins_failing(stop_after=1):
         try:
             with np.errstate(all="ignore"):
                 pin()
-        except Exception as e:          # an assertion, or the mistake breaking a contract
+        except (Exception, pytest.fail.Exception) as e:   # an assertion, a pytest.raises miss,
+            # or the mistake breaking a contract
             failed.append(f"{pin.__name__}: {type(e).__name__}")
             if len(failed) >= stop_after:
                 break
