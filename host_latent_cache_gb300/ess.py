@@ -38,7 +38,7 @@ EXPORTS = (
     "ess_indexer_topk", "ess_stage_misses", "ess_sparse_mla_decode", "ess_step",
     "ess_step_profiled", "ess_step_host",
     "ess_pipeline_step", "ess_pool_get_state", "ess_pool_set_state", "ess_pool_get_rows",
-    "ess_pool_read_stats", "ess_pool_poll", "ess_pool_kernel_launches",
+    "ess_pool_read_stats", "ess_pool_poll", "ess_pool_kernel_launches", "ess_prefill_plan",
 )
 
 
@@ -105,6 +105,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "ess_pool_read_stats": [P, I, ctypes.POINTER(ess_stats), I],
         "ess_pool_poll": [P, P],
         "ess_pool_kernel_launches": [P, ctypes.POINTER(ctypes.c_int64)],
+        "ess_prefill_plan": [I, P, I, I, P, P, P],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -306,3 +307,15 @@ def ess_pool_kernel_launches(pool) -> int:
 
 def ess_pool_poll(pool, stream=None) -> int:
     return load().ess_pool_poll(pool, _stream(stream))
+
+
+def ess_prefill_plan(onload_layer_map, rotating: int = 3, shared_copy: bool = False):
+    """Binding table of the prefill layer schedule: (buffer, load_at,
+    reuse_after) as int32 arrays, one entry per layer."""
+    import numpy as np
+    m = np.ascontiguousarray(onload_layer_map, dtype=np.int32)
+    L = int(m.shape[0])
+    outs = [np.zeros(L, dtype=np.int32) for _ in range(3)]
+    check(load().ess_prefill_plan(L, m.ctypes.data, int(rotating), int(bool(shared_copy)),
+                                  *[o.ctypes.data for o in outs]), "ess_prefill_plan")
+    return tuple(outs)

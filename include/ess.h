@@ -323,6 +323,30 @@ ess_status ess_pool_read_stats(ess_pool* pool, int layer, ess_stats* out, int re
  * copies are not kernels and are not counted). */
 ess_status ess_pool_kernel_launches(const ess_pool* pool, int64_t* count);
 
+/* Binding table of the prefill layer schedule with whole-layer device
+ * buffers ([FO] "prefill side": B0 pinned to layer 0, B1..B3 rotating through
+ * a binding table, a buffer reused only after its layer's compute and
+ * write-back, layer onload_layer_map[i] prefetched at layer i's scheduling
+ * point).  Host code only; it plans, it moves nothing.
+ *   n_layers          L >= 1
+ *   onload_layer_map  host int32 [L]: the layer (1..L-1) prefetched at layer
+ *                     i's scheduling point, or -1; a layer no entry names is
+ *                     loaded up front
+ *   rotating          buffers besides B0 (the page uses 3)
+ *   shared_copy       1 when loads and write-backs share one serial copy
+ *                     stream (a layer's write-back is then issued after the
+ *                     prefetch at its own scheduling point)
+ * Outputs (host int32 [L]): buffer[l] (0 = B0, else 1..rotating, bound
+ * round-robin in load order), load_at[l] (the scheduling point that issues
+ * l's load, -1 for up front and for layer 0), reuse_after[l] (the layer whose
+ * release l's load waits for, or -1).
+ * Errors: ESS_ERR_INVALID_ARG for a bad argument, a layer loaded twice, or a
+ * load that would wait for a layer whose write-back is not yet issued (the
+ * buffer would still be held). */
+ess_status ess_prefill_plan(int32_t n_layers, const int32_t* onload_layer_map, int32_t rotating,
+                            int32_t shared_copy, int32_t* buffer, int32_t* load_at,
+                            int32_t* reuse_after);
+
 /* Synchronise stream, return the first device-side error since the last
  * poll (ESS_OK if none) and clear it. */
 ess_status ess_pool_poll(ess_pool* pool, ess_stream_t stream);
