@@ -39,6 +39,7 @@ EXPORTS = (
     "ess_step_profiled", "ess_step_host",
     "ess_pipeline_step", "ess_pool_get_state", "ess_pool_set_state", "ess_pool_get_rows",
     "ess_pool_read_stats", "ess_pool_poll", "ess_pool_kernel_launches", "ess_prefill_plan",
+    "ess_compact_rows",
 )
 
 
@@ -106,6 +107,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "ess_pool_poll": [P, P],
         "ess_pool_kernel_launches": [P, ctypes.POINTER(ctypes.c_int64)],
         "ess_prefill_plan": [I, P, I, I, P, P, P],
+        "ess_compact_rows": [P, ctypes.c_int64, P],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -319,3 +321,13 @@ def ess_prefill_plan(onload_layer_map, rotating: int = 3, shared_copy: bool = Fa
     check(load().ess_prefill_plan(L, m.ctypes.data, int(rotating), int(bool(shared_copy)),
                                   *[o.ctypes.data for o in outs]), "ess_prefill_plan")
     return tuple(outs)
+
+
+def ess_compact_rows(rows_bf16_bits):
+    """bf16 bits [n][576] (numpy uint16) -> compact rows uint8 [n][656]."""
+    import numpy as np
+    rows = np.ascontiguousarray(rows_bf16_bits, dtype=np.uint16).reshape(-1, 576)
+    out = np.zeros((rows.shape[0], 656), dtype=np.uint8)
+    check(load().ess_compact_rows(rows.ctypes.data, rows.shape[0], out.ctypes.data),
+          "ess_compact_rows")
+    return out

@@ -323,6 +323,19 @@ ess_status ess_pool_read_stats(ess_pool* pool, int layer, ess_stats* out, int re
  * copies are not kernels and are not counted). */
 ess_status ess_pool_kernel_launches(const ess_pool* pool, int64_t* count);
 
+/* Encode latent rows as compact 656-byte rows ("ESS: Latent-Cache Offload",
+ * the ~656-byte host transfers of its FlashTrans + UVA row and its 16.8% /
+ * 83.2% indexer/latent byte split).  Layout (a reading; the page gives only
+ * the size): bytes 0..511 the 512 latent values as e4m3 in four tiles of 128,
+ * bytes 512..527 one little-endian float32 scale per tile, bytes 528..655 the
+ * 64 RoPE values as bf16.  A tile's scale is fl32(amax / 448) (1 for an
+ * all-zero tile); a value's code is e4m3(fl32(x / scale)), nearest with ties
+ * to the even code, saturating at +-448, sign kept.  Host code only.
+ *   rows_bf16  host bf16 [n_rows][576]
+ *   out        host uint8 [n_rows][656]
+ * Errors: ESS_ERR_INVALID_ARG for n_rows < 0 or a null buffer. */
+ess_status ess_compact_rows(const uint16_t* rows_bf16, int64_t n_rows, uint8_t* out);
+
 /* Binding table of the prefill layer schedule with whole-layer device
  * buffers ([FO] "prefill side": B0 pinned to layer 0, B1..B3 rotating through
  * a binding table, a buffer reused only after its layer's compute and
