@@ -25,6 +25,8 @@ ESS_ERR_DEVICE_CHECK = 7
 
 ESS_FP8_E4M3 = 0
 ESS_BF16 = 1
+
+ESS_EVICT_LRU, ESS_EVICT_RANDOM, ESS_EVICT_SCORE, ESS_EVICT_LIM = range(4)
 ESS_MISS_FUSED = 0
 ESS_MISS_STAGED = 1
 
@@ -39,7 +41,7 @@ EXPORTS = (
     "ess_step_profiled", "ess_step_host",
     "ess_pipeline_step", "ess_pool_get_state", "ess_pool_set_state", "ess_pool_get_rows",
     "ess_pool_read_stats", "ess_pool_poll", "ess_pool_kernel_launches", "ess_prefill_plan",
-    "ess_compact_rows",
+    "ess_compact_rows", "ess_replay_misses",
 )
 
 
@@ -108,6 +110,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "ess_pool_kernel_launches": [P, ctypes.POINTER(ctypes.c_int64)],
         "ess_prefill_plan": [I, P, I, I, P, P, P],
         "ess_compact_rows": [P, ctypes.c_int64, P],
+        "ess_replay_misses": [I, I, P, P, P, I, I, I, ctypes.c_uint64, ctypes.c_int64, P, P],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -331,3 +334,27 @@ def ess_compact_rows(rows_bf16_bits):
     check(load().ess_compact_rows(rows.ctypes.data, rows.shape[0], out.ctypes.data),
           "ess_compact_rows")
     return out
+
+
+def ess_replay_misses(trace, T: int, C: int, policy: int, scores=None, seed: int = 0,
+                      request: int = 0):
+    """trace[s][m]: the tokens way m selected at step s; scores[s][m]: the
+    way's scores of all T tokens (Score policy).  Returns (union_misses,
+    way_misses) per step as int32 arrays."""
+    import numpy as np
+    n_steps = len(trace)
+    n_ways = len(trace[0]) if n_steps else 1
+    lists = [np.asarray(w, dtype=np.int32) for ways in trace for w in ways]
+    offsets = np.zeros(len(lists) + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum([x.shape[0] for x in lists])
+    tokens = np.concatenate(lists) if lists else np.zeros(1, np.int32)
+    sc = None
+    if scores is not None:
+        sc = np.ascontiguousarray(np.asarray(scores, dtype=np.float32).reshape(n_steps, n_ways, T))
+    um = np.zeros(max(n_steps, 1), dtype=np.int32)
+    wm = np.zeros(max(n_steps, 1), dtype=np.int32)
+    check(load().ess_replay_misses(n_steps, n_ways, offsets.ctypes.data, tokens.ctypes.data,
+                                   None if sc is None else sc.ctypes.data, T, C, policy,
+                                   seed & ((1 << 64) - 1), request, um.ctypes.data,
+                                   wm.ctypes.data), "ess_replay_misses")
+    return um[:n_steps], wm[:n_steps]

@@ -323,6 +323,35 @@ ess_status ess_pool_read_stats(ess_pool* pool, int layer, ess_stats* out, int re
  * copies are not kernels and are not counted). */
 ess_status ess_pool_kernel_launches(const ess_pool* pool, int64_t* count);
 
+/* Victim orders of ess_replay_misses. */
+enum { ESS_EVICT_LRU = 0, ESS_EVICT_RANDOM = 1, ESS_EVICT_SCORE = 2, ESS_EVICT_LIM = 3 };
+
+/* Replay one request's trace of selections with an eviction policy and count
+ * its misses ([FO] "evaluation": the decode ablation's offline simulator and
+ * Figure 8, which replays the same top-k trace with Random, LRU, Score and
+ * LIM eviction).  Host code only; the decode kernels always use LRU.
+ *   offsets, tokens  the selections in CSR form: way m of step s selected
+ *                    tokens[offsets[s*n_ways+m] .. offsets[s*n_ways+m+1])
+ *   scores           host float [n_steps][n_ways][T], the ways' scores of every
+ *                    token (ESS_EVICT_SCORE only; else may be NULL)
+ *   T, C             tokens and hot-pool slots of the request
+ *   policy           ESS_EVICT_*; seed and request key the Random draws
+ * Each step: hits are stamped; the slots not holding a selected token are the
+ * candidates, empty slots first in slot order, then resident ones by LRU
+ * (last use), Random (a SplitMix64 draw per slot keyed by seed, request and
+ * step), Score (the token's score this step, maximum over the ways) or LIM
+ * (slot order), ties to the lower slot; the i-th miss in token order takes
+ * the i-th candidate.
+ * Outputs (host int32 [n_steps]): union_misses (distinct rows loaded) and
+ * way_misses (selected tokens not resident before the step, summed over the
+ * ways, as the page's figure counts them).
+ * Errors: ESS_ERR_INVALID_ARG for bad arguments or a token outside [0, T);
+ * ESS_ERR_CAPACITY when a step selects more than C distinct tokens. */
+ess_status ess_replay_misses(int32_t n_steps, int32_t n_ways, const int64_t* offsets,
+                             const int32_t* tokens, const float* scores, int32_t T, int32_t C,
+                             int32_t policy, uint64_t seed, int64_t request,
+                             int32_t* union_misses, int32_t* way_misses);
+
 /* Encode latent rows as compact 656-byte rows ("ESS: Latent-Cache Offload",
  * the ~656-byte host transfers of its FlashTrans + UVA row and its 16.8% /
  * 83.2% indexer/latent byte split).  Layout (a reading; the page gives only
