@@ -33,3 +33,18 @@ def test_defaults_meet_the_timing_rules(monkeypatch):
 
 def test_cpu_model_is_named():
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_layer_roofline_terms():
+    # 138.4 MB of keys and 15,000 hit rows at 6,781 GB/s, a 100 us step
+    r = bench.layer_roofline(138_412_032, 15_000, 1_200, 100.0, 6781.1,
+                             idx_flops=2 * 64 * 128 * 8 * 131072, idx_us=45.0, bf16_tflops=1907.9)
+    r_idx = 138_412_032 / 6781.1e9 * 1e6
+    r_hit = 15_000 * 1152 / 6781.1e9 * 1e6
+    assert abs(r["R_us"] - max(r_idx, r_hit)) < 1e-9 and abs(r["frac"] - r["R_us"] / 100.0) < 1e-12
+    assert abs(r["additive_us"] - (r_idx + r_hit)) < 1e-9 and r["additive_frac"] > r["frac"]
+    assert r["miss_bytes_per_step"] == 1_200 * 1152
+    t = r["indexer_tensor"]
+    assert abs(t["achieved_tflops"] - 2 * 64 * 128 * 8 * 131072 / 45e-6 / 1e12) < 1e-9
+    assert t["peak_tflops"] == 2 * 1907.9 and 0 < t["frac"] < 0.2
+    assert "indexer_tensor" not in bench.layer_roofline(1, 1, 0, 1.0, 1.0)
