@@ -38,6 +38,9 @@ ess_status check_config(const ess_config* c) {
   // the miss union never exceeds min(M*k, T) rows, so it always fits
   const long long need = std::min<long long>(static_cast<long long>(c->mtp) * c->k, c->max_T);
   if (c->C < need) return ESS_ERR_CAPACITY;
+  // every kernel's shared memory must fit one CTA
+  if (indexer_smem_need(*c) > kMaxSmemPerCta || select_smem_need(*c) > kMaxSmemPerCta)
+    return ESS_ERR_UNSUPPORTED;
   return ESS_OK;
 }
 

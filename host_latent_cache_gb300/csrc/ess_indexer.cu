@@ -338,6 +338,13 @@ size_t indexer_smem_bytes(int NP, int HB) {
 
 }  // namespace
 
+// Shared memory of one indexer CTA with the fused score histogram (the step's
+// configuration; the kernel has no static shared memory).
+size_t indexer_smem_need(const ess_config& c) {
+  const int NP = ((c.mtp * c.idx_heads + 31) / 32) * 32;
+  return indexer_smem_bytes(NP, c.mtp * kHistBins);
+}
+
 cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, const float* w,
                            float* scores, bool with_hist, cudaStream_t st) {
   const ess_config& c = p.cfg;

@@ -148,6 +148,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Largest shared memory one CTA of a kernel asks for under a config, and the
+// per-CTA limit of this architecture (227 KiB).  Configs above it are refused
+// when validated, instead of failing at launch.
+constexpr size_t kMaxSmemPerCta = 232448;
+size_t indexer_smem_need(const ess_config& c);
+size_t select_smem_need(const ess_config& c);
+
 // Kernel launchers (one per kernel file).  They assume validated arguments.
 // with_hist: also accumulate the per-(request, way) score histogram in the
 // pool's scratch (it must be zero; the selection kernel zeroes it after use).

@@ -1094,6 +1094,44 @@ cudaError_t launch_order_reset(const ess_pool& p, int layer, cudaStream_t st) {
   return e;
 }
 
+namespace {
+
+// Shared-memory sizes of the selection kernel for a largest request length
+// T_hmax: the per-CTA token range, the list capacities, and the bytes of the
+// lists (fixed) and of the staged scores (res_bytes).
+struct SelSizes {
+  int nl, c_local, lcap, gcap;
+  size_t res_bytes, fixed;
+};
+
+constexpr size_t kSelKeysBudget = 160 * 1024;   // leaves room for the static shared state
+
+SelSizes sel_sizes(const ess_config& c, int T_hmax) {
+  SelSizes z;
+  z.nl = (T_hmax + CL - 1) / CL;
+  z.nl = ((z.nl + 3) / 4) * 4;
+  if (z.nl < 4) z.nl = 4;
+  z.c_local = (c.C + CL - 1) / CL;
+  const int MK = c.mtp * c.k;
+  z.lcap = z.nl < MK ? z.nl : MK;   // the union of one CTA's tokens never exceeds this
+  z.lcap = (z.lcap + 3) / 4 * 4;    // keeps the arrays after the list 16-byte aligned
+  z.gcap = 4096;
+  z.res_bytes = static_cast<size_t>(c.mtp) * z.nl * 4;
+  z.fixed = static_cast<size_t>(z.lcap) * (9 + 4 * c.mtp) + static_cast<size_t>(z.c_local) * 5 +
+            static_cast<size_t>(z.gcap) * 5 + 64;
+  return z;
+}
+
+}  // namespace
+
+// Largest shared memory (static + dynamic) one selection CTA can ask for over
+// every request length up to max_T: the lists grow with the length, and the
+// staged scores are used only while they fit the budget.
+size_t select_smem_need(const ess_config& c) {
+  const SelSizes z = sel_sizes(c, c.max_T);
+  return sizeof(SelShared) + (z.fixed > kSelKeysBudget ? z.fixed : kSelKeysBudget);
+}
+
 cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, bool hist_given,
                           int32_t* topk_idx, int32_t* topk_slot, int32_t* n_miss_way,
                           int32_t* miss_tok, int32_t* miss_slot, int32_t* n_miss, cudaStream_t st) {
@@ -1123,20 +1161,14 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
   a.k = c.k;
   a.T = c.max_T;
   a.C = c.C;
-  int nl = (L.T_hmax + CL - 1) / CL;
-  nl = ((nl + 3) / 4) * 4;
-  if (nl < 4) nl = 4;
-  a.n_local = nl;
-  a.c_local = (c.C + CL - 1) / CL;
-  const int MK = c.mtp * c.k;
-  a.lcap = nl < MK ? nl : MK;   // the union of one CTA's tokens never exceeds this
-  a.lcap = (a.lcap + 3) / 4 * 4; // keeps the arrays after the list 16-byte aligned
-  a.gcap = 4096;
-  const size_t res_bytes = static_cast<size_t>(c.mtp) * nl * 4;
-  const size_t fixed = static_cast<size_t>(a.lcap) * (9 + 4 * c.mtp) +
-                       static_cast<size_t>(a.c_local) * 5 + static_cast<size_t>(a.gcap) * 5 + 64;
-  const size_t budget = 160 * 1024;   // leaves room for the static shared state
-  a.resident = (res_bytes + fixed <= budget) ? 1 : 0;
+  const SelSizes z = sel_sizes(c, L.T_hmax);
+  a.n_local = z.nl;
+  a.c_local = z.c_local;
+  a.lcap = z.lcap;
+  a.gcap = z.gcap;
+  const size_t res_bytes = z.res_bytes;
+  const size_t fixed = z.fixed;
+  a.resident = (res_bytes + fixed <= kSelKeysBudget) ? 1 : 0;
   size_t kb = a.resident ? res_bytes : 0;
   kb = (kb + 15) / 16 * 16;
   a.keys_bytes = static_cast<uint32_t>(kb);

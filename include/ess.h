@@ -84,7 +84,8 @@ typedef struct {
   int32_t C;           /* hot-pool slots per request and layer ([FO] C_b)     */
   int32_t page;        /* host page size in tokens (block-table granularity)  */
   int32_t k;           /* top-k per way ([FO]: k = 2048)                      */
-  int32_t mtp;         /* M ways per step, 1..4 ([FO]: MTP3 = 4 ways)         */
+  int32_t mtp;         /* M ways per step, 1..4 ([FO]: MTP3 = 4 ways), as far */
+                       /* as one CTA's shared memory allows (see below)      */
   int32_t idx_heads;   /* H_I                                                 */
   int32_t idx_dim;     /* d_I; a key row must be 128 bytes                    */
   int32_t idx_dtype;   /* ESS_FP8_E4M3 (d_I = 128) or ESS_BF16 (d_I = 64)     */
@@ -112,8 +113,14 @@ const char* ess_status_string(ess_status s);
 /* Bytes of device workspace that ess_pool_create needs for cfg.
  * Covers, per layer: cache_slots [B][T] int32, slot_token [B][C] int32,
  * last_used [B][C] int32, step [B] int32, the hot pool [B][C][D] bf16, the
- * ring of appended rows [B][2 * page][D] bf16 and counters; plus scratch shared by the layers (scores, selection lists,
- * attention partials, staging for ess_step_host).
+ * ring of appended rows [B][2 * page][D] bf16 and counters; plus scratch
+ * shared by the layers (scores, selection lists, attention partials,
+ * staging for ess_step_host).
+ * A config whose kernels would need more shared memory per CTA than the GPU
+ * has (227 KiB) is refused with ESS_ERR_UNSUPPORTED: the indexer keeps two
+ * 16 KiB score histograms per way, so 3 ways at 64 indexer heads or 4 ways
+ * at any width do not fit, and 4 ways at k = 2048 overflow the selection
+ * kernel's lists.
  * Errors: ESS_ERR_INVALID_ARG / ESS_ERR_UNSUPPORTED for a bad cfg. */
 ess_status ess_pool_device_bytes(const ess_config* cfg, size_t* bytes);
 

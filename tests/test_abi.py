@@ -73,6 +73,21 @@ def test_config_validation(lib, field, value, code):
     assert lib.ess_pool_device_bytes(ctypes.byref(c), ctypes.byref(n)) == code
 
 
+def test_config_beyond_shared_memory_is_refused(lib):
+    # 4 ways at k=2048 (selection lists) and 3 ways at 64 indexer heads
+    # (indexer histograms and queries) need more than one CTA's 227 KiB
+    def code(cfg):
+        c = ess_config_of(cfg)
+        n = ctypes.c_size_t(0)
+        return lib.ess_pool_device_bytes(ctypes.byref(c), ctypes.byref(n))
+    base = W.multilayer().replace(layers=1, C=16384)
+    assert code(base) == ess.ESS_OK                                   # 2 ways
+    assert code(base.replace(mtp=4)) == ess.ESS_ERR_UNSUPPORTED
+    assert code(base.replace(mtp=3)) == ess.ESS_ERR_UNSUPPORTED
+    assert code(base.replace(mtp=3, idx_heads=32, k=256, C=4096)) == ess.ESS_OK
+    assert code(W.tiny().replace(mtp=4)) == ess.ESS_ERR_UNSUPPORTED   # four 16 KiB histograms x 2
+
+
 def test_create_rejects_bad_workspace_without_touching_a_gpu(lib):
     c = ess_config_of(W.tiny())
     h = ctypes.c_void_p(0)
