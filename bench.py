@@ -59,6 +59,9 @@ def parse():
     ap.add_argument("--workload", default="long_128k", choices=sorted(W.ALL_CONFIGS))
     ap.add_argument("--miss-mode", default="fused", choices=["fused", "staged"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-link", action="store_true", help="skip the host-link measurement")
+    ap.add_argument("--empty-pool", action="store_true",
+                    help="time from an empty pool instead of filling it first")
     ap.add_argument("--cpu-steps", type=int, default=48)
     ap.add_argument("--overlap-steps", type=int, default=24)
     ap.add_argument("--pipeline", type=int, default=0,
@@ -297,24 +300,29 @@ def bench_reference(args, cfg, rank, world):
 
 
 # ---------------------------------------------------------------- our arm
-def measure_overlap(cfg, ld, n_steps, stream, host_buffers):
+def measure_overlap(cfg, ld, n_steps, stream, host_buffers, qs=None, start_state=None):
     """T_copy (staging kernel), T_SFA (attention with every row in the pool)
     and T_fused (attention that reads misses from host memory itself), per
     step, and OverlapRatio = (T_copy + T_SFA - T_fused) / T_copy.  A fused pool
     runs the steps first, then a staged pool replays the same inputs from the
-    same empty state (identical selections and misses), one pool at a time;
-    both read the latent cache of the main session's host buffer.  Events
-    between the kernels stop them from launching early, as in the separate
-    calls these timings stand for."""
+    same state (identical selections and misses), one pool at a time; both
+    read the latent cache of the main session's host buffer.  With a start
+    state (the main session's steady state) and its query stream both pools
+    begin where the timed run ended; otherwise they start empty and the first
+    steps, which still fill the pool, are reported apart.  Events between the
+    kernels stop them from launching early, as in the separate calls these
+    timings stand for."""
     import torch
     from host_latent_cache_gb300 import ess
     from host_latent_cache_gb300.session import Session
-    qs = W.QueryStream(cfg)
+    qs = qs if qs is not None else W.QueryStream(cfg)
     wts = W.head_weights(cfg, ld.w)
     steps = [qs.next() for _ in range(n_steps)]
     res, outs = {}, {}
     for mode in (ess.ESS_MISS_FUSED, ess.ESS_MISS_STAGED):
         sess = Session(cfg, [ld], miss_mode=mode, host_buffers=host_buffers)
+        if start_state is not None:
+            sess.set_state(0, start_state)
         ins = [sess.device_inputs(enc, wts, qm) for (_, enc, qm) in steps]
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in steps]
         nm = torch.zeros(len(steps), dtype=torch.int64, device=sess.device)
@@ -340,22 +348,30 @@ def measure_overlap(cfg, ld, n_steps, stream, host_buffers):
         sess.close()
     fz, sg = res[ess.ESS_MISS_FUSED], res[ess.ESS_MISS_STAGED]
     assert [r[0] for r in fz] == [r[0] for r in sg]
-    # the first steps after the first fill still miss heavily (the pool has not
-    # settled into the drift's working set): they are reported apart
-    settle = min(4, len(fz) - 1)
+    # from an empty pool the first steps after the first fill still miss
+    # heavily (the pool has not settled into the drift's working set): they are
+    # reported apart
+    settle = 0 if start_state is not None else min(4, len(fz) - 1)
     rng = range(settle, len(fz))
     tc = statistics.mean(sg[i][1] for i in rng)
     ts = statistics.mean(sg[i][2] for i in rng)
     tf = statistics.mean(fz[i][2] for i in rng)
-    return {"steps": len(rng), "settling_steps_dropped": settle,
-            "miss_rows_per_step": statistics.mean(fz[i][0] for i in rng),
-            "t_copy_us": 1e3 * tc, "t_sfa_us": 1e3 * ts, "t_fused_us": 1e3 * tf,
-            "overlap_ratio": (tc + ts - tf) / tc if tc > 0 else None,
-            "speedup_vs_copy_then_attend": (tc + ts) / tf if tf > 0 else None,
-            "first_fill": {"miss_rows": fz[0][0], "t_copy_us": 1e3 * sg[0][1],
-                           "t_sfa_us": 1e3 * sg[0][2], "t_fused_us": 1e3 * fz[0][2]},
-            "outputs_identical": bool(torch.equal(outs[ess.ESS_MISS_FUSED],
-                                                  outs[ess.ESS_MISS_STAGED]))}
+    out = {"steps": len(rng), "settling_steps_dropped": settle,
+           "start": "steady state of the timed run" if start_state is not None else "empty pool",
+           "miss_rows_per_step": statistics.mean(fz[i][0] for i in rng),
+           "t_copy_us": 1e3 * tc, "t_sfa_us": 1e3 * ts, "t_fused_us": 1e3 * tf,
+           "overlap_ratio": (tc + ts - tf) / tc if tc > 0 else None,
+           "speedup_vs_copy_then_attend": (tc + ts) / tf if tf > 0 else None,
+           "per_step_us": {"miss_rows": [fz[i][0] for i in rng],
+                           "fused": [round(1e3 * fz[i][2], 1) for i in rng],
+                           "copy": [round(1e3 * sg[i][1], 1) for i in rng],
+                           "sfa": [round(1e3 * sg[i][2], 1) for i in rng]},
+           "outputs_identical": bool(torch.equal(outs[ess.ESS_MISS_FUSED],
+                                                 outs[ess.ESS_MISS_STAGED]))}
+    if settle:
+        out["first_fill"] = {"miss_rows": fz[0][0], "t_copy_us": 1e3 * sg[0][1],
+                             "t_sfa_us": 1e3 * sg[0][2], "t_fused_us": 1e3 * fz[0][2]}
+    return out
 
 
 # what the indexer kernel's device code is built from: its own file, the
@@ -367,19 +383,24 @@ INDEXER_CONSTANTS = "ess_internal.h"
 
 
 def layer_roofline(idx_bytes, hit_rows, miss_rows, step_us, hbm_gbs, idx_flops=None,
-                   idx_us=None, bf16_tflops=None):
-    """The layer's roofline terms: R = max(indexer bytes, hit bytes) / HBM
-    bandwidth against the step, the stricter additive form (both streams
-    through HBM one after the other), the miss bytes over the host link
-    (reported; no measured link peak is recorded, so it stays out of R), and
-    the indexer's fraction of the FP8 tensor peak (the measured bf16 peak
-    times the nominal FP8/bf16 ratio of 2)."""
+                   idx_us=None, bf16_tflops=None, link_gbs=None):
+    """The layer's roofline terms: R = max(indexer bytes / HBM, hit bytes /
+    HBM, miss bytes / host link) against the step; the stricter additive form
+    (indexer and hit bytes through HBM one after the other, plus the miss
+    bytes over the link); and the indexer's fraction of the FP8 tensor peak
+    (the measured bf16 peak times the nominal FP8/bf16 ratio of 2).  Without
+    a measured link peak the miss term is left out and only reported."""
     r_idx = idx_bytes / (hbm_gbs * 1e9) * 1e6
     r_hit = hit_rows * ROW_BYTES / (hbm_gbs * 1e9) * 1e6
-    out = {"R_us": max(r_idx, r_hit), "step_us": step_us, "frac": max(r_idx, r_hit) / step_us,
-           "additive_us": r_idx + r_hit, "additive_frac": (r_idx + r_hit) / step_us,
-           "terms_us": {"indexer": r_idx, "hits": r_hit},
-           "miss_rows_per_step": miss_rows, "miss_bytes_per_step": miss_rows * ROW_BYTES}
+    miss_bytes = miss_rows * ROW_BYTES
+    r_miss = miss_bytes / (link_gbs * 1e9) * 1e6 if link_gbs else 0.0
+    R = max(r_idx, r_hit, r_miss)
+    add = r_idx + r_hit + r_miss
+    out = {"R_us": R, "step_us": step_us, "frac": R / step_us,
+           "additive_us": add, "additive_frac": add / step_us,
+           "terms_us": {"indexer": r_idx, "hits": r_hit, "misses_link": r_miss},
+           "link_peak_gbs": link_gbs,
+           "miss_rows_per_step": miss_rows, "miss_bytes_per_step": miss_bytes}
     if idx_flops is not None and idx_us and bf16_tflops:
         achieved = idx_flops / (idx_us * 1e-6) / 1e12
         peak = 2.0 * bf16_tflops
@@ -422,6 +443,76 @@ def indexer_traffic(cfg):
         return None
 
 
+def measure_link(host_buf, n_host_rows, device, stream, reps=5):
+    """Host-link rates through the library's own gather kernel (16-byte loads
+    by the GPU's threads, as the miss path reads) and through the copy engine
+    (cudaMemcpyAsync from pinned memory), each timed with CUDA events over
+    `reps` launches after one untimed launch.  Returns GB/s figures; the
+    largest sequential rate is the link peak of the layer roofline."""
+    import torch
+    from host_latent_cache_gb300 import ess
+    res = {}
+    n_seq = min(n_host_rows, (256 << 20) // ROW_BYTES)
+    dst = torch.empty((n_seq, ROW_BYTES), dtype=torch.uint8, device=device)
+    bad = torch.zeros(1, dtype=torch.int32, device=device)
+    g = torch.Generator().manual_seed(4242)
+
+    def timed(fn, nbytes):
+        fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+    res["gather_seq_gbs"] = timed(
+        lambda: ess.ess_host_gather(host_buf, n_host_rows, ROW_BYTES, None, n_seq, dst, bad,
+                                    stream), n_seq * ROW_BYTES)
+    for n in (16384, n_seq):
+        rows = torch.randint(0, n_host_rows, (n,), generator=g, dtype=torch.int64).to(device)
+        res[f"gather_random_{n}_rows_gbs"] = timed(
+            lambda: ess.ess_host_gather(host_buf, n_host_rows, ROW_BYTES, rows, n, dst, bad,
+                                        stream), n * ROW_BYTES)
+    hsrc = torch.empty(n_seq * ROW_BYTES, dtype=torch.uint8).pin_memory()
+    dflat = dst.view(-1)
+    res["copy_engine_h2d_gbs"] = timed(lambda: dflat.copy_(hsrc, non_blocking=True),
+                                       n_seq * ROW_BYTES)
+    torch.cuda.synchronize()
+    assert int(bad.item()) == 0
+    res["bytes_per_sequential_read"] = n_seq * ROW_BYTES
+    res["peak_gbs"] = max(res["gather_seq_gbs"], res["copy_engine_h2d_gbs"])
+    res["peak_source"] = ("measured in this run: the larger of the sequential gather kernel "
+                          "and the copy engine")
+    return res
+
+
+def fill_pool(sess, qs, wts, stream, max_steps=1024, check_every=16):
+    """Runs decode steps (untimed) until every request's hot pool is full, so
+    that the timed steps see the steady state of the FlashOffloading analysis
+    ("decode side (1)": loads equal evictions once the C slots are taken).
+    Returns (steps run, fraction of slots resident)."""
+    import numpy as np
+    from host_latent_cache_gb300 import ess
+    C, B = sess.cfg.C, sess.cfg.batch
+    T = np.asarray(sess.T[0].numpy())
+    full = float(np.minimum(T, C).sum())
+    n, occ = 0, 0.0
+    while n < max_steps:
+        for _ in range(check_every):
+            _, enc, qm = qs.next()
+            qd, wd, qmd = sess.device_inputs(enc, wts, qm)
+            ess.ess_step(sess.pool, 0, qd, wd, qmd, sess.out, stream)
+            n += 1
+        _, st, _, _ = sess.state(0)
+        occ = float((st >= 0).sum()) / full if full else 1.0
+        if occ >= 1.0:
+            break
+    return n, occ
+
+
 def bench_ours(args, cfg, rank, world, local_rank):
     import torch
     from host_latent_cache_gb300 import build as B
@@ -446,6 +537,10 @@ def bench_ours(args, cfg, rank, world, local_rank):
     qs = W.QueryStream(cfg_r)
     n_total = args.warmup + 3 * args.steps
     wts = W.head_weights(cfg_r, ld.w)
+    stream = torch.cuda.current_stream()
+    # steady state: the pool is filled by real decode steps before the warm-up
+    fill_steps, occupancy = (fill_pool(sess, qs, wts, stream) if not args.empty_pool
+                             else (0, 0.0))
     dev_inputs, host_inputs = [], []
     for s in range(n_total):
         q, enc, qm = qs.next()
@@ -457,7 +552,6 @@ def bench_ours(args, cfg, rank, world, local_rank):
             hqm = torch.from_numpy(np.ascontiguousarray(qm).view(np.int16)).pin_memory()
             host_inputs.append((hq, hw, hqm))
     out_host = torch.empty(tuple(sess.out.shape), dtype=torch.float32).pin_memory()
-    stream = torch.cuda.current_stream()
     nsteps = args.steps
 
     def make_events(n, k):
@@ -515,11 +609,11 @@ def bench_ours(args, cfg, rank, world, local_rank):
     sel_ms = [e[1].elapsed_time(e[2]) for e in ev]
     att_ms = [e[2].elapsed_time(e[3]) for e in ev]
 
-    # OverlapRatio of the fused miss path: fused and staged pools stepped in
-    # lockstep on the same inputs (identical state trajectories)
-    overlap = None
-    if args.overlap_steps > 0 and world == 1:
-        overlap = measure_overlap(cfg_r, ld, args.overlap_steps, stream, sess.host)
+    # host-link rates (the miss term of the roofline), on this session's host copy
+    link = None
+    if rank == 0 and not args.no_link:
+        link = measure_link(sess.host[0], cfg_r.batch * W.t_max_of(cfg_r), sess.device, stream)
+
 
     # end to end through the public C ABI with host buffers
     torch.cuda.synchronize()
@@ -533,6 +627,15 @@ def bench_ours(args, cfg, rank, world, local_rank):
     torch.cuda.synchronize()
     assert sess.poll(stream) == ess.ESS_OK
     e2e_ms = e_start.elapsed_time(e_end)
+
+    # OverlapRatio of the fused miss path: fused and staged pools stepped in
+    # lockstep on the same inputs (identical state trajectories), from the
+    # state the main pool has reached, with the queries that follow
+    overlap = None
+    if args.overlap_steps > 0 and world == 1:
+        cs_, st_, lu_, sp_ = sess.state(0)
+        overlap = measure_overlap(cfg_r, ld, args.overlap_steps, stream, sess.host, qs=qs,
+                                  start_state=W.PoolState(cs_, st_, lu_, sp_))
 
     elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], dist, device="cuda")
     units_step = cfg.batch * cfg.mtp            # one decode layer of the workload per step
@@ -558,18 +661,30 @@ def bench_ours(args, cfg, rank, world, local_rank):
         step_us = elapsed_ms * 1e3 / nsteps
         idx_flops = 2 * cfg.idx_heads * cfg.idx_dim * Tsum * cfg.mtp
         traffic = indexer_traffic(cfg)
+        link_peak = link["peak_gbs"] if link else None
+        att_avg_ms = statistics.mean(att_ms)
+        if link is not None:
+            # miss bytes the fused attention moved over the link per step, over
+            # the attention kernel's time (attention + merge, event-timed)
+            link["achieved_fused_attention_gbs"] = (miss_rows * ROW_BYTES
+                                                    / (att_avg_ms * 1e-3) / 1e9)
+            link["achieved_frac_of_peak"] = link["achieved_fused_attention_gbs"] / link_peak
         result = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": nsteps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / nsteps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
-            "config": config_json(cfg, world, args.miss_mode),
+            "config": dict(config_json(cfg, world, args.miss_mode),
+                           pool_fill_steps=fill_steps, pool_occupancy_at_warmup=occupancy,
+                           pool_state="steady (full before the warm-up)" if occupancy >= 1.0
+                           else "filling"),
             "roofline": {"bound": "hbm", "kernel": "indexer (a1)", "achieved": achieved,
                          "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                          "traffic": traffic, "peak_source": peak_src,
                          "algorithmic_bytes_per_launch": idx_bytes},
             "layer_roofline": layer_roofline(idx_bytes, hit_rows, miss_rows, step_us, hbm_peak,
                                              idx_flops, idx_avg_ms * 1e3,
-                                             peaks.get("bf16_tflops")),
+                                             peaks.get("bf16_tflops"), link_peak),
+            "link": link,
             "kernels_ms": {"indexer": statistics.mean(idx_ms), "select": statistics.mean(sel_ms),
                            "attention": statistics.mean(att_ms)},
             "hit_rate": stats.hits / max(stats.hits + stats.misses, 1),

@@ -339,6 +339,7 @@ ess_status ess_append(ess_pool* pool, int layer, const void* latent_row, const v
     tmax = T > tmax ? T : tmax;
   }
   L.n_appended = n;
+  L.append_pending = true;
   L.total_tiles = tiles;
   L.T_hmax = tmax;
   return ESS_OK;
@@ -533,7 +534,28 @@ ess_status ess_pool_set_state(ess_pool* pool, int layer, const int32_t* cache_sl
     int32_t* dst = L.order + (static_cast<size_t>(sp[b] & 1) * B + b) * c.C;
     if (cudaMemcpy(dst, ord.data(), c.C * 4, cudaMemcpyHostToDevice) != cudaSuccess) return ESS_ERR_CUDA;
   }
+  // the rows of the resident tokens come from the authoritative host copy
+  if (L.bound) {
+    if (launch_refill(*pool, layer, nullptr) != cudaSuccess) return ESS_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return ESS_ERR_CUDA;
+  }
   return ESS_OK;
+}
+
+ess_status ess_host_gather(const void* host_rows, int64_t n_host_rows, int32_t row_bytes,
+                           const int64_t* rows, int64_t n_rows, void* dst, int32_t* bad_row,
+                           ess_stream_t stream) {
+  if (!host_rows || !dst || n_host_rows < 0 || n_rows < 0 || row_bytes <= 0 || row_bytes % 16 ||
+      !aligned16(host_rows) || !aligned16(dst))
+    return ESS_ERR_INVALID_ARG;
+  if (!rows && n_rows > n_host_rows) return ESS_ERR_INVALID_ARG;
+  void* dev_alias = nullptr;
+  if (cudaHostGetDevicePointer(&dev_alias, const_cast<void*>(host_rows), 0) != cudaSuccess) {
+    cudaGetLastError();
+    return ESS_ERR_INVALID_ARG;  // not pinned / mapped host memory
+  }
+  return cuda_status(launch_host_gather(dev_alias, rows, n_rows, n_host_rows, row_bytes, dst,
+                                        bad_row, static_cast<cudaStream_t>(stream)));
 }
 
 ess_status ess_pool_get_rows(ess_pool* pool, int layer, void* rows_host) {

@@ -453,6 +453,59 @@ __global__ void __launch_bounds__(256) stage_kernel(const int32_t* __restrict__ 
     if (lane + 32 * q < kRowBytes / 16) d[lane + 32 * q] = r[q];
 }
 
+// Reload the rows of every resident token from the host copy (or the ring of
+// appended rows) into its pool slot: slot s of request b holds token
+// slot_token[b][s] after a restored state.  One warp per slot.
+__global__ void __launch_bounds__(256) refill_kernel(const int32_t* __restrict__ slot_token,
+                                                     const int32_t* __restrict__ Tb,
+                                                     const int32_t* __restrict__ page_table,
+                                                     const uint16_t* __restrict__ host,
+                                                     const uint16_t* __restrict__ tail,
+                                                     const int32_t* __restrict__ T0,
+                                                     uint16_t* __restrict__ pool, int C, int T,
+                                                     int page, int npages, int* status) {
+  const int b = blockIdx.y;
+  const int s = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (s >= C) return;
+  const int t = slot_token[static_cast<size_t>(b) * C + s];
+  if (t < 0) return;
+  const int tb = Tb[b];
+  int prow = t;
+  if (page_table && t < tb)
+    prow = page_table[static_cast<size_t>(b) * npages + t / page] * page + t % page;
+  if (t >= tb || prow < 0 || prow >= T) {
+    if (lane == 0) set_status(status, ESS_ERR_DEVICE_CHECK);
+    return;
+  }
+  const int tail_lo = max(T0[b], (tb / page - 1) * page);
+  const uint4* src = reinterpret_cast<const uint4*>(
+      t >= tail_lo ? tail + (static_cast<size_t>(b) * 2 * page + t % (2 * page)) * kRowDim
+                   : host + (static_cast<size_t>(b) * T + prow) * kRowDim);
+  uint4* d = reinterpret_cast<uint4*>(pool + (static_cast<size_t>(b) * C + s) * kRowDim);
+  for (int q = lane; q < kRowBytes / 16; q += 32) d[q] = src[q];
+}
+
+// Rows of a pinned host array -> device memory, one warp per row, 16-byte
+// loads: the miss path's access pattern, for measuring the host link.
+__global__ void __launch_bounds__(256) host_gather_kernel(const uint4* __restrict__ host,
+                                                          const int64_t* __restrict__ rows,
+                                                          int64_t n_rows, int64_t n_host_rows,
+                                                          int vec_per_row, uint4* __restrict__ dst,
+                                                          int* status) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (i >= n_rows) return;
+  const int64_t r = rows ? rows[i] : i;
+  if (r < 0 || r >= n_host_rows) {
+    if (lane == 0 && status) atomicCAS(status, 0, 1);
+    return;
+  }
+  const uint4* s = host + r * vec_per_row;
+  uint4* d = dst + i * vec_per_row;
+  for (int q = lane; q < vec_per_row; q += 32) d[q] = s[q];
+}
+
 size_t attn_smem_bytes() { return 1024 + kRowsBytes + kQBytes + 24 * 8 + 16; }
 
 }  // namespace
@@ -519,6 +572,30 @@ cudaError_t launch_stage(const ess_pool& p, int layer, const int32_t* miss_tok,
                  c.max_T / c.page, p.scr.status);
   if (e == cudaSuccess) count_launch(p);
   return e;
+}
+
+cudaError_t launch_refill(const ess_pool& p, int layer, cudaStream_t st) {
+  const ess_config& c = p.cfg;
+  const Layer& L = p.layers[layer];
+  dim3 grid((c.C + 7) / 8, c.batch);
+  refill_kernel<<<grid, 256, 0, st>>>(L.slot_token, L.T_dev, L.page_table, L.host_latent, L.tail,
+                                      L.T0_dev, L.pool, c.C, c.max_T, c.page, c.max_T / c.page,
+                                      p.scr.status);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch(p);
+  return e;
+}
+
+cudaError_t launch_host_gather(const void* host_dev, const int64_t* rows, int64_t n_rows,
+                               int64_t n_host_rows, int row_bytes, void* dst, int* status,
+                               cudaStream_t st) {
+  if (n_rows == 0) return cudaSuccess;
+  const int64_t blocks = (n_rows + 7) / 8;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  host_gather_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      static_cast<const uint4*>(host_dev), rows, n_rows, n_host_rows, row_bytes / 16,
+      static_cast<uint4*>(dst), status);
+  return cudaGetLastError();
 }
 
 }  // namespace ess

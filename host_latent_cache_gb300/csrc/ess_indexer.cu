@@ -8,10 +8,13 @@
 //
 // Persistent, warp-specialised kernel, one CTA per SM:
 //   warp 0     (one lane) streams 128-token key tiles (128 B per token) with
-//              TMA into a 6-stage ring, and at each request boundary starts
-//              asynchronous loads of that request's queries (TMA, 128B
-//              swizzle) and head weights (bulk copy) without pausing the
-//              key stream;
+//              TMA into a ring of as many 16 KB stages as shared memory holds
+//              (up to 12), and at each request boundary starts asynchronous
+//              loads of that request's queries (TMA, 128B swizzle) and head
+//              weights (bulk copy) without pausing the key stream.  Key tiles
+//              of tokens present at the bind depend on no earlier kernel, so
+//              the first ring's worth is requested before the wait for the
+//              previous grid, overlapping the stream's ramp-up with its tail;
 //   warp 1     (one lane) issues tcgen05.mma: D[128 tokens][N] = K_tile * Q^T
 //              with e4m3 (kind::f8f6f4) or bf16 (kind::f16) inputs and fp32
 //              accumulators in TMEM, N = ways x heads padded to 32;
@@ -20,7 +23,8 @@
 //              head weights and the key scale, stores the score and counts it
 //              in a shared-memory histogram of the top 12 bits of its ordered
 //              key, which is added to a per-(request, way) global histogram
-//              at the end of each request's run of tiles.
+//              at the end of each request's run of tiles (one histogram per
+//              way, flushed and cleared between two barriers).
 // The key tiles are the only large HBM stream; the kernel is bound by HBM
 // bandwidth (about 132 B per token and request).
 #include "ess_device.cuh"
@@ -38,9 +42,10 @@ struct IdxArgs {
   uint32_t* ghist;           // [B][M][kHistBins] or null
   int* status;
   int B, M, HI, NP, T, total_tiles, A;
+  int S;                     // key-ring stages
+  int early;                 // 1: no append since the last indexer launch on this layer
 };
 
-constexpr int S = kIdxStages;
 constexpr uint32_t kTileBytes = kIdxTile * kKeyRowBytes;  // 16 KB
 
 __device__ __forceinline__ int find_request(const int32_t* tile_off, int B, int g) {
@@ -58,20 +63,22 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const int NP = a.NP;
   const int A = a.A;
+  const int S = a.S;
   uint8_t* kst = smem;                                   // S x 16 KB key tiles
   uint8_t* qbuf = kst + S * kTileBytes;                  // 2 x NP x 128 B queries
   float* wbuf = reinterpret_cast<float*>(qbuf + 2 * NP * 128);  // 2 x NP weights
-  uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + 2 * NP);   // 2 x M x kHistBins
+  uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + 2 * NP);   // M x kHistBins
   const int HB = a.ghist ? a.M * kHistBins : 0;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(hist + 2 * HB);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(hist + HB);
   uint64_t* full = bars;
   uint64_t* empty = full + S;
   uint64_t* accf = empty + S;
   uint64_t* acce = accf + 4;
   uint64_t* qfull = acce + 4;
   uint64_t* qempty = qfull + 2;
-  uint64_t* epdone = qempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epdone + 2);
+  uint64_t* epdone = qempty + 2;      // every epilogue thread has counted its tiles
+  uint64_t* fldone = epdone + 2;      // the histogram is flushed and clear again
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fldone + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* consumed = abort_flag + 1;
 
@@ -97,12 +104,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       mbar_init(smem_u32(&qfull[i]), 1);
       mbar_init(smem_u32(&qempty[i]), 1 + 256);
       mbar_init(smem_u32(&epdone[i]), 256);
+      mbar_init(smem_u32(&fldone[i]), 256);
     }
     *abort_flag = 0;
     *consumed = 0;
     fence_mbar_init();
   }
-  for (int i = tid; i < 2 * HB; i += kIdxThreads) hist[i] = 0;
+  for (int i = tid; i < HB; i += kIdxThreads) hist[i] = 0;
   for (int i = tid; i < 2 * NP; i += kIdxThreads) wbuf[i] = 0.0f;
   uint32_t ncols = 32;
   while (ncols < static_cast<uint32_t>(A * NP)) ncols <<= 1;
@@ -118,7 +126,24 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // everything above touched only this CTA's shared memory and TMEM
+  // everything above touched only this CTA's shared memory and TMEM.  Early
+  // mode: no append kernel has run on this layer since its last indexer, so
+  // the tile prefix and the key rows of the first tiles are final already and
+  // the first ring's worth of key tiles is requested before the wait.
+  int n_early = 0;
+  if (warp == 0 && a.early) {
+    if (lane == 0) {
+      int b = find_request(a.tile_off, a.B, g0);
+      for (int g = g0; g < g1 && n_early < S; ++g, ++n_early) {
+        while (b + 1 < a.B && g >= a.tile_off[b + 1]) ++b;
+        const int j = g - a.tile_off[b];
+        mbar_arrive_expect_tx(smem_u32(&full[n_early]), kTileBytes);
+        tma_load_2d(smem_u32(kst + n_early * kTileBytes), &kmap, smem_u32(&full[n_early]), 0,
+                    b * a.T + j * kIdxTile);
+      }
+    }
+    n_early = __shfl_sync(0xffffffffu, n_early, 0);
+  }
   pdl_wait_previous();
   pdl_launch_dependents();
 
@@ -155,7 +180,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         cur_b = b;
       }
       int w_ok = 1;
-      if (lane == 0) {
+      if (lane == 0 && it >= n_early) {
         const int s = it % S;
         if (it >= S) w_ok = mbar_wait(smem_u32(&empty[s]), ((it / S) - 1) & 1, abort_flag) ? 1 : 0;
         if (w_ok) {
@@ -175,7 +200,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     }
     // drain: wait (bounded) for every issued tile load to land
     if (lane == 0 && *abort_flag) {
-      for (int i = *consumed; i < it; ++i) mbar_wait(smem_u32(&full[i % S]), (i / S) & 1, nullptr);
+      const int issued = it > n_early ? it : n_early;
+      for (int i = *consumed; i < issued; ++i)
+        mbar_wait(smem_u32(&full[i % S]), (i / S) & 1, nullptr);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
@@ -225,6 +252,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     int cur_b = -1, seg = -1, it = 0;
     int Tcur = 0;
     bool ok = true;
+    // 64-column TMEM loads when no chunk straddles two ways
+    const bool wide = (NP % 64 == 0) && (a.M == 1 || a.HI % 64 == 0);
     for (int g = g0; g < g1 && ok; ++g, ++it) {
       while (b + 1 < a.B && g >= a.tile_off[b + 1]) ++b;
       const int j = g - a.tile_off[b];
@@ -266,7 +295,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             p3 = fmaf(w4.w, fmaxf(v[i + 3], 0.0f), p3);
           }
           sm[0] = (p0 + p1) + (p2 + p3);
-        } else {
+        } else if (wide) {
           for (int c = 0; c < NP / 64; ++c) {
             float v[64];
             tmem_ld64(taddr + c * 64, v);
@@ -280,8 +309,29 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
               p3 = fmaf(w4.w, fmaxf(v[i + 3], 0.0f), p3);
             }
             const float part = (p0 + p1) + (p2 + p3);
-            // columns n = c*64 + i belong to way n / H_I (H_I % 32 == 0 or M == 1)
+            // columns n = c*64 + i belong to way n / H_I (here H_I % 64 == 0 or M == 1)
             const int m = (a.M == 1) ? 0 : (c * 64) / a.HI;
+            if (m == 0) sm[0] += part;
+            else if (m == 1) sm[1] += part;
+            else if (m == 2) sm[2] += part;
+            else sm[3] += part;
+          }
+        } else {
+          // 32-column chunks: a way of 32 heads, or N = 96 / 160 / 224
+          for (int c = 0; c < NP / 32; ++c) {
+            float v[32];
+            tmem_ld32(taddr + c * 32, v);
+            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 w4 = *reinterpret_cast<const float4*>(wq + c * 32 + i);
+              p0 = fmaf(w4.x, fmaxf(v[i], 0.0f), p0);
+              p1 = fmaf(w4.y, fmaxf(v[i + 1], 0.0f), p1);
+              p2 = fmaf(w4.z, fmaxf(v[i + 2], 0.0f), p2);
+              p3 = fmaf(w4.w, fmaxf(v[i + 3], 0.0f), p3);
+            }
+            const float part = (p0 + p1) + (p2 + p3);
+            const int m = (a.M == 1) ? 0 : (c * 32) / a.HI;   // H_I % 32 == 0 when M > 1
             if (m == 0) sm[0] += part;
             else if (m == 1) sm[1] += part;
             else if (m == 2) sm[2] += part;
@@ -291,13 +341,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         tc_fence_before();
         mbar_arrive(smem_u32(&acce[acc]));
         if (in_range) {
-          uint32_t* hseg = hist + (seg & 1) * HB;
 #pragma unroll
           for (int m = 0; m < kMaxWays; ++m) {   // unrolled: sm stays in registers
             if (m >= a.M) break;
             const float sv = __fmul_rn(sm[m], sc) + 0.0f;  // one rounding; +0 for a zero score
             a.scores[(static_cast<size_t>(b) * a.M + m) * a.T + t] = sv;
-            if (HB) atomicAdd(hseg + m * kHistBins + (float_key(sv) >> 20), 1u);
+            if (HB) atomicAdd(hist + m * kHistBins + (float_key(sv) >> 20), 1u);
           }
         }
       }
@@ -309,15 +358,17 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (HB) {
           mbar_arrive(smem_u32(&epdone[seg & 1]));
           if (!mbar_wait(smem_u32(&epdone[seg & 1]), (seg >> 1) & 1, abort_flag)) break;
-          uint32_t* hseg = hist + (seg & 1) * HB;
           uint32_t* gh = a.ghist + static_cast<size_t>(b) * a.M * kHistBins;
           for (int i = te; i < HB; i += 256) {
-            const uint32_t v = hseg[i];
+            const uint32_t v = hist[i];
             if (v) {
               atomicAdd(gh + i, v);
-              hseg[i] = 0;
+              hist[i] = 0;
             }
           }
+          // nobody counts the next request's tokens before the clear is complete
+          mbar_arrive(smem_u32(&fldone[seg & 1]));
+          if (!mbar_wait(smem_u32(&fldone[seg & 1]), (seg >> 1) & 1, abort_flag)) break;
         }
       }
     }
@@ -331,18 +382,26 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   }
 }
 
-size_t indexer_smem_bytes(int NP, int HB) {
-  return 1024 + static_cast<size_t>(S) * kTileBytes + 2u * NP * 128 + 2u * NP * 4 +
-         2u * HB * 4 + (2 * S + 8 + 6) * 8 + 16;
+size_t indexer_smem_bytes(int S, int NP, int HB) {
+  return 1024 + static_cast<size_t>(S) * kTileBytes + 2u * NP * 128 + 2u * NP * 4 + HB * 4u +
+         (2 * S + 8 + 8) * 8 + 16;
+}
+
+// Largest key ring (at most kIdxMaxStages) that fits one CTA beside the
+// queries, weights and histogram.
+int indexer_stages(int NP, int HB) {
+  int S = kIdxMaxStages;
+  while (S > kIdxMinStages && indexer_smem_bytes(S, NP, HB) > kMaxSmemPerCta) --S;
+  return S;
 }
 
 }  // namespace
 
-// Shared memory of one indexer CTA with the fused score histogram (the step's
-// configuration; the kernel has no static shared memory).
+// Shared memory of one indexer CTA with the fused score histogram and the
+// shortest ring (the kernel has no static shared memory).
 size_t indexer_smem_need(const ess_config& c) {
   const int NP = ((c.mtp * c.idx_heads + 31) / 32) * 32;
-  return indexer_smem_bytes(NP, c.mtp * kHistBins);
+  return indexer_smem_bytes(kIdxMinStages, NP, c.mtp * kHistBins);
 }
 
 cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, const float* w,
@@ -366,13 +425,16 @@ cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, cons
   a.T = c.max_T;
   a.total_tiles = L.total_tiles;
   a.A = 512 / a.NP < 4 ? 512 / a.NP : 4;
+  const int HB = with_hist ? c.mtp * kHistBins : 0;
+  a.S = indexer_stages(a.NP, HB);
+  a.early = L.append_pending ? 0 : 1;
   CUtensorMap qmap;
   if (!encode_map_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_idx, kKeyRowBytes,
                      static_cast<uint64_t>(c.batch) * c.mtp * c.idx_heads, kKeyRowBytes,
                      kKeyRowBytes, static_cast<uint32_t>(a.NP)))
     return cudaErrorInvalidValue;
   const int grid = L.total_tiles < p.num_sms ? L.total_tiles : p.num_sms;
-  const size_t smem = indexer_smem_bytes(a.NP, with_hist ? c.mtp * kHistBins : 0);
+  const size_t smem = indexer_smem_bytes(a.S, a.NP, HB);
   cudaError_t e;
   if (c.idx_dtype == ESS_FP8_E4M3) {
     e = cudaFuncSetAttribute(indexer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -385,7 +447,11 @@ cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, cons
     if (e != cudaSuccess) return e;
     e = launch_pdl(indexer_kernel<false>, dim3(grid), dim3(kIdxThreads), smem, st, L.kmap, qmap, a);
   }
-  if (e == cudaSuccess) count_launch(p);
+  if (e == cudaSuccess) {
+    count_launch(p);
+    // this launch waits for any append before it, so the next one may load early
+    p.layers[layer].append_pending = false;
+  }
   return e;
 }
 

@@ -21,7 +21,8 @@ constexpr int kKeyRowBytes = 128;     // one indexer key row
 
 constexpr int kIdxThreads = 320;      // 10 warps: TMA, MMA, 2 groups of 4 epilogue warps
 constexpr int kHistBins = 4096;       // score histogram on the top 12 bits of the ordered key
-constexpr int kIdxStages = 6;         // key-tile ring
+constexpr int kIdxMaxStages = 12;     // key-tile ring: as many 16 KB stages as fit, up to 12
+constexpr int kIdxMinStages = 4;
 constexpr int kIdxTile = 128;         // tokens per tile (MMA M)
 
 constexpr int kSelCluster = 8;        // CTAs per request in the selection kernel
@@ -51,6 +52,9 @@ struct Layer {
   uint16_t* tail = nullptr;       // [B][2 * page][D] bf16, token t at row t % (2 * page)
   std::vector<int32_t> T0_host;   // host copy of T0_dev
   int32_t n_appended = 0;         // tokens appended to every request since the bind
+  // an append kernel was launched after the last indexer launch: the next
+  // indexer must wait for it before reading tile prefixes or key rows
+  mutable bool append_pending = false;
   CUtensorMap kmap;               // keys as [B*T rows][128 B], 128x128 boxes, 128B swizzle
   // state
   int32_t* cache_slots = nullptr; // [B][T]
@@ -175,6 +179,13 @@ cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
                              const int32_t* topk_idx, const int32_t* topk_slot, float* out,
                              bool misses_staged, bool early, cudaStream_t st);
 cudaError_t launch_reset(const ess_pool& p, int layer, cudaStream_t st);
+// rows of a device-mapped pinned host array -> dst (rows NULL: rows 0..n-1);
+// a row index outside [0, n_host_rows) sets *status (when given) to 1
+cudaError_t launch_host_gather(const void* host_dev, const int64_t* rows, int64_t n_rows,
+                               int64_t n_host_rows, int row_bytes, void* dst, int* status,
+                               cudaStream_t st);
+// reload the pool rows of every resident token from the host copy
+cudaError_t launch_refill(const ess_pool& p, int layer, cudaStream_t st);
 cudaError_t launch_append(const ess_pool& p, int layer, const void* latent, const void* key,
                           const float* key_scale, cudaStream_t st);
 

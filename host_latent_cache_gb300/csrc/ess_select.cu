@@ -1216,11 +1216,10 @@ static __device__ __align__(256) unsigned char g_select_scratch[kSelectStaticScr
 std::mutex g_scratch_mu;
 void* g_scratch_addr[128] = {nullptr};
 
-cudaError_t select_scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+// dev must be the current device: the lookup returns the current device's copy.
+cudaError_t select_scratch_address(int dev, void** out) {
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  cudaError_t e;
   std::lock_guard<std::mutex> g(g_scratch_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
@@ -1252,8 +1251,13 @@ extern "C" ess_status ess_select_manage_noalloc(ess_pool* pool, int layer, const
   const size_t hist_bytes = align256_sz(bm * kHistBins * sizeof(uint32_t));
   const size_t vlist_bytes = align256_sz(bm * c.k * sizeof(int32_t));
   if (hist_bytes + vlist_bytes > kSelectStaticScratchBytes) return ESS_ERR_OOM;
+  // the array is looked up (and later used) on the pool's device, which must be
+  // the current one, as for every call on the pool
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return ESS_ERR_CUDA;
+  if (cur != pool->device) return ESS_ERR_INVALID_ARG;
   void* base = nullptr;
-  if (select_scratch_address(&base) != cudaSuccess) return ESS_ERR_CUDA;
+  if (select_scratch_address(pool->device, &base) != cudaSuccess) return ESS_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the histogram is accumulated with atomics, so it must start at zero
   if (cudaMemsetAsync(base, 0, hist_bytes, st) != cudaSuccess) return ESS_ERR_CUDA;

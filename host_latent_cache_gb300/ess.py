@@ -41,7 +41,7 @@ EXPORTS = (
     "ess_step_profiled", "ess_step_host",
     "ess_pipeline_step", "ess_pool_get_state", "ess_pool_set_state", "ess_pool_get_rows",
     "ess_pool_read_stats", "ess_pool_poll", "ess_pool_kernel_launches", "ess_prefill_plan",
-    "ess_compact_rows", "ess_replay_misses",
+    "ess_compact_rows", "ess_replay_misses", "ess_host_gather",
 )
 
 
@@ -111,6 +111,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "ess_prefill_plan": [I, P, I, I, P, P, P],
         "ess_compact_rows": [P, ctypes.c_int64, P],
         "ess_replay_misses": [I, I, P, P, P, I, I, I, ctypes.c_uint64, ctypes.c_int64, P, P],
+        "ess_host_gather": [P, ctypes.c_int64, I, P, ctypes.c_int64, P, P, P],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -358,3 +359,12 @@ def ess_replay_misses(trace, T: int, C: int, policy: int, scores=None, seed: int
                                    seed & ((1 << 64) - 1), request, um.ctypes.data,
                                    wm.ctypes.data), "ess_replay_misses")
     return um[:n_steps], wm[:n_steps]
+
+
+def ess_host_gather(host_rows, n_host_rows: int, row_bytes: int, rows, n_rows: int, dst,
+                    bad_row=None, stream=None) -> None:
+    """Rows of pinned host memory (a HostBuffer or pinned tensor) into the
+    device tensor dst; rows is a device int64 tensor or None (sequential)."""
+    check(load().ess_host_gather(_p(host_rows), int(n_host_rows), int(row_bytes), _p(rows),
+                                 int(n_rows), _p(dst), _p(bad_row), _stream(stream)),
+          "ess_host_gather")

@@ -126,6 +126,13 @@ class Session:
         ess.ess_pool_get_state(self.pool, layer, cs, st, lu, sp)
         return cs.numpy(), st.numpy(), lu.numpy(), sp.numpy()
 
+    def set_state(self, layer, state: "W.PoolState"):
+        """Start the layer from a given pool state; the rows of its resident
+        tokens are reloaded from the host copy."""
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))
+        ess.ess_pool_set_state(self.pool, layer, t(state.cache_slots), t(state.slot_token),
+                               t(state.last_used), t(state.step))
+
     def pool_rows(self, layer):
         """The hot pool of a layer as uint16 [B][C][576] (synchronous copy)."""
         rows = torch.empty((self.cfg.batch, self.cfg.C, W.ROW_DIM), dtype=torch.int16)

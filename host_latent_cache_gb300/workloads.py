@@ -308,6 +308,44 @@ def gen_layer(cfg: WorkloadConfig, layer: int = 0, want_latent: bool = True) -> 
     return LayerData(keys, scale, w, latent, host, pages, Ts, app_keys, app_scale)
 
 
+_TID_STATE = 8
+
+
+@dataclass
+class PoolState:
+    """A hot-pool state to start from (one layer): cache_slots [B][T_max],
+    slot_token [B][C], last_used [B][C] int32 and step [B] int32."""
+    cache_slots: np.ndarray
+    slot_token: np.ndarray
+    last_used: np.ndarray
+    step: np.ndarray
+
+
+def full_pool_state(cfg: WorkloadConfig, ld: LayerData, layer: int = 0,
+                    age: int = 8) -> PoolState:
+    """A pool that has been running for `age` steps and is full: every
+    request holds min(C, T_b) distinct tokens drawn at random, in random
+    slots, each last used at a random earlier step in [0, age) (so many slots
+    share a stamp), and the step counter stands at `age`.  Empty slots (when
+    T_b < C) keep token -1 and stamp -1.  A draw of inputs only: which slots
+    a step evicts from it is left to the code under test."""
+    B, C, Tm = cfg.batch, cfg.C, t_max_of(cfg)
+    cs = np.full((B, Tm), -1, np.int32)
+    st = np.full((B, C), -1, np.int32)
+    lu = np.full((B, C), -1, np.int32)
+    sp = np.full(B, age, np.int32)
+    for b in range(B):
+        r = _rng(cfg.seed, _TID_STATE, layer, b)
+        Tb = int(ld.T[b])
+        n = min(C, Tb)
+        toks = r.choice(Tb, size=n, replace=False).astype(np.int32)
+        slots = r.permutation(C)[:n].astype(np.int32)
+        st[b, slots] = toks
+        cs[b, toks] = slots
+        lu[b, slots] = r.integers(0, age, size=n).astype(np.int32)
+    return PoolState(cs, st, lu, sp)
+
+
 def appended_token(cfg: WorkloadConfig, ld: LayerData, i: int):
     """Inputs of the i-th decode append (token T_b + i of each request):
     latent rows uint16 [B][576], key rows uint8 [B][row_bytes], scales

@@ -117,10 +117,11 @@ const char* ess_status_string(ess_status s);
  * shared by the layers (scores, selection lists, attention partials,
  * staging for ess_step_host).
  * A config whose kernels would need more shared memory per CTA than the GPU
- * has (227 KiB) is refused with ESS_ERR_UNSUPPORTED: the indexer keeps two
- * 16 KiB score histograms per way, so 3 ways at 64 indexer heads or 4 ways
- * at any width do not fit, and 4 ways at k = 2048 overflow the selection
- * kernel's lists.
+ * has (227 KiB) is refused with ESS_ERR_UNSUPPORTED.  The indexer fits every
+ * width up to 4 ways x 64 heads (its key ring shortens to make room for the
+ * queries and one 16 KiB score histogram per way); the selection kernel's
+ * per-CTA lists grow with min(max_T / 8, mtp * k), so 4 ways at k = 2048 fit
+ * up to max_T = 32768 (the pages' MTP3 at the V3.2 shape) but not at 65536.
  * Errors: ESS_ERR_INVALID_ARG / ESS_ERR_UNSUPPORTED for a bad cfg. */
 ess_status ess_pool_device_bytes(const ess_config* cfg, size_t* bytes);
 
@@ -228,7 +229,8 @@ ess_status ess_select_manage(ess_pool* pool, int layer, const float* scores,
  * library, which every GPU that loads the library keeps until the process
  * exits.  It calls no allocator.
  *   - Returns ESS_ERR_OOM, launching nothing, when the scratch needed exceeds
- *     the 2 MiB array.
+ *     the 2 MiB array, and ESS_ERR_INVALID_ARG when the current device is not
+ *     the pool's (each device has its own copy of the array).
  *   - The first call on a device looks up the array's device address; make
  *     that first call before any stream capture.
  *   - All calls share the one array: calls that overlap on the GPU (different
@@ -311,12 +313,37 @@ ess_status ess_pipeline_step(ess_pool* const* pools, int n_pools, int n_layers,
 ess_status ess_pool_get_state(ess_pool* pool, int layer, int32_t* cache_slots,
                               int32_t* slot_token, int32_t* last_used, int32_t* step);
 
-/* Overwrite the bookkeeping of one layer from host buffers (synchronous).
- * The caller keeps it consistent (cache_slots and slot_token inverse maps)
- * and the pool rows of resident tokens filled. */
+/* Overwrite the bookkeeping of one layer from host buffers (synchronous):
+ * resume from a saved state, or start from a full pool.  Any argument may be
+ * NULL to keep that part.  The caller keeps it consistent (cache_slots and
+ * slot_token inverse maps, last_used < step).  The LRU order is rebuilt from
+ * last_used, and, when the layer is bound, the pool row of every resident
+ * token (slot_token >= 0) is reloaded from the bound host copy, so that hits
+ * read the right rows ([FO] "architecture": the host copy is the
+ * authoritative one).  A resident token at or past T_b is reported by
+ * ess_pool_poll as ESS_ERR_DEVICE_CHECK and its row is left as it was. */
 ess_status ess_pool_set_state(ess_pool* pool, int layer, const int32_t* cache_slots,
                               const int32_t* slot_token, const int32_t* last_used,
                               const int32_t* step);
+
+/* Gather rows of a pinned host array into device memory with 16-byte loads
+ * issued by the GPU's own threads over the host link: the access pattern of
+ * the miss path ([FO] "decode side (2)": misses are read from host memory
+ * straight on chip).  Used to measure the link's sequential and random-row
+ * rates, the host-link term of the layer's roofline.
+ *   host_rows    pinned host [n_host_rows][row_bytes] (ess_host_alloc or any
+ *                mapped pinned memory), 16-byte aligned
+ *   row_bytes    a multiple of 16
+ *   rows         device int64 [n_rows]: the host row of each output row, or
+ *                NULL for rows 0..n_rows-1 (a sequential read)
+ *   dst          device [n_rows][row_bytes], 16-byte aligned
+ *   bad_row      device int32, or NULL: set to 1 by a row index outside
+ *                [0, n_host_rows) (that row is skipped)
+ * Errors: ESS_ERR_INVALID_ARG for a bad argument or memory that is not
+ * pinned and mapped. */
+ess_status ess_host_gather(const void* host_rows, int64_t n_host_rows, int32_t row_bytes,
+                           const int64_t* rows, int64_t n_rows, void* dst, int32_t* bad_row,
+                           ess_stream_t stream);
 
 /* Copy the hot pool of one layer, [B][C][D] bf16, to a host buffer
  * (synchronous); rows of empty slots hold whatever was last written. */

@@ -31,14 +31,28 @@ def assert_attn_close(got, want, what=""):
 class Pair:
     """A GPU session and an oracle per layer, fed identical inputs."""
 
-    def __init__(self, cfg: W.WorkloadConfig, layers: int = 1, miss_mode=ess.ESS_MISS_FUSED):
+    def __init__(self, cfg: W.WorkloadConfig, layers: int = 1, miss_mode=ess.ESS_MISS_FUSED,
+                 lds=None):
         self.cfg = cfg
-        self.lds = [W.gen_layer(cfg, l) for l in range(layers)]
+        self.lds = lds if lds is not None else [W.gen_layer(cfg, l) for l in range(layers)]
+        layers = len(self.lds)
         self.sess = Session(cfg, self.lds, miss_mode)
         self.orc = [O.OracleLayer(ld.T, cfg.C, cfg.k, cfg.sm_scale) for ld in self.lds]
         self.qs = [W.QueryStream(cfg, l) for l in range(layers)]
         self.keys32 = [W.decode_keys(cfg, ld.idx_keys).astype(np.float32) for ld in self.lds]
         self.errs = []
+        self.evicted = []   # per step: resident tokens evicted, summed over requests
+
+    def prime_full(self, layer=0, age=8):
+        """Both sides start from the same full pool (W.full_pool_state)."""
+        ps = W.full_pool_state(self.cfg, self.lds[layer], layer, age)
+        self.sess.set_state(layer, ps)
+        for b in range(self.cfg.batch):
+            Tb = int(self.lds[layer].T[b])
+            self.orc[layer].state[b] = O.CacheState(ps.cache_slots[b, :Tb].copy(),
+                                                    ps.slot_token[b].copy(),
+                                                    ps.last_used[b].copy(), int(ps.step[b]))
+        return ps
 
     def oracle_inputs(self, layer):
         ld = self.lds[layer]
@@ -71,9 +85,12 @@ class Pair:
         assert st == ess.ESS_OK, ess.status_string(st)
         keyf, latf = self.oracle_inputs(layer)
         ld = self.lds[layer]
+        tok_before = [st_.slot_token.copy() for st_ in self.orc[layer].state]
         r = self.orc[layer].step(q.astype(np.float64), w.astype(np.float64), keyf, ld.idx_scale,
                                  W.bf16_bits_to_float(qm).astype(np.float64), latf,
                                  keep_scores=check_scores)
+        self.evicted.append(sum(int(np.count_nonzero(tok_before[b][r.miss_slot[b]] >= 0))
+                                for b in range(cfg.batch)))
         if check_scores:
             for b in range(cfg.batch):
                 Tb = int(ld.T[b])

@@ -74,18 +74,22 @@ def test_config_validation(lib, field, value, code):
 
 
 def test_config_beyond_shared_memory_is_refused(lib):
-    # 4 ways at k=2048 (selection lists) and 3 ways at 64 indexer heads
-    # (indexer histograms and queries) need more than one CTA's 227 KiB
+    # the indexer fits every width up to 4 ways x 64 heads (one 16 KiB
+    # histogram per way, a shorter key ring); the selection's per-CTA lists
+    # grow with min(T/8, M*k), so 4 ways at k=2048 fit the V3.2 length but not
+    # the 65536-token one
     def code(cfg):
         c = ess_config_of(cfg)
         n = ctypes.c_size_t(0)
         return lib.ess_pool_device_bytes(ctypes.byref(c), ctypes.byref(n))
     base = W.multilayer().replace(layers=1, C=16384)
     assert code(base) == ess.ESS_OK                                   # 2 ways
-    assert code(base.replace(mtp=4)) == ess.ESS_ERR_UNSUPPORTED
-    assert code(base.replace(mtp=3)) == ess.ESS_ERR_UNSUPPORTED
-    assert code(base.replace(mtp=3, idx_heads=32, k=256, C=4096)) == ess.ESS_OK
-    assert code(W.tiny().replace(mtp=4)) == ess.ESS_ERR_UNSUPPORTED   # four 16 KiB histograms x 2
+    assert code(base.replace(mtp=3, C=16384)) == ess.ESS_OK
+    assert code(base.replace(mtp=4)) == ess.ESS_ERR_UNSUPPORTED       # selection lists
+    v32 = W.v32_32k()
+    assert code(v32.replace(mtp=4, C=8192)) == ess.ESS_OK             # the pages' MTP3: 4 ways
+    assert code(v32.replace(mtp=3, C=8192)) == ess.ESS_OK
+    assert code(W.tiny().replace(mtp=4, idx_heads=32)) == ess.ESS_OK
 
 
 def test_create_rejects_bad_workspace_without_touching_a_gpu(lib):

@@ -15,8 +15,17 @@ def test_throughput_counts_one_layer_per_step():
         assert bench.config_json(cfg, 1, "fused")["layers"] == 1
 
 
+def _recorded_digest(name):
+    import os
+    with open(os.path.join(bench.ROOT, "profiles", f"indexer_{name}.txt")) as f:
+        for line in f:
+            if line.startswith("source_digest"):
+                return line.split("=", 1)[1].strip()
+
+
 def test_traffic_comes_from_the_profile_while_sources_match(monkeypatch):
     cfg = W.long_128k()
+    monkeypatch.setattr(bench, "indexer_source_digest", lambda: _recorded_digest(cfg.name))
     t = bench.indexer_traffic(cfg)
     assert isinstance(t, int) and t > 138_412_032            # at least the algorithmic bytes
     monkeypatch.setattr(bench, "indexer_source_digest", lambda: "0" * 16)
@@ -48,3 +57,18 @@ def test_layer_roofline_terms():
     assert abs(t["achieved_tflops"] - 2 * 64 * 128 * 8 * 131072 / 45e-6 / 1e12) < 1e-9
     assert t["peak_tflops"] == 2 * 1907.9 and 0 < t["frac"] < 0.2
     assert "indexer_tensor" not in bench.layer_roofline(1, 1, 0, 1.0, 1.0)
+
+
+def test_layer_roofline_link_term():
+    # 1,200 miss rows over a 200 GB/s link take 6.9 us: above the hit term,
+    # below the indexer's 20.4 us; the additive form adds all three
+    r = bench.layer_roofline(138_412_032, 15_000, 1_200, 100.0, 6781.1, link_gbs=200.0)
+    r_idx = 138_412_032 / 6781.1e9 * 1e6
+    r_hit = 15_000 * 1152 / 6781.1e9 * 1e6
+    r_miss = 1_200 * 1152 / 200e9 * 1e6
+    assert abs(r["terms_us"]["misses_link"] - r_miss) < 1e-9
+    assert abs(r["R_us"] - max(r_idx, r_hit, r_miss)) < 1e-9
+    assert abs(r["additive_us"] - (r_idx + r_hit + r_miss)) < 1e-9
+    # a slow link makes the miss term the bound
+    r2 = bench.layer_roofline(138_412_032, 15_000, 1_200, 100.0, 6781.1, link_gbs=10.0)
+    assert abs(r2["R_us"] - 1_200 * 1152 / 10e9 * 1e6) < 1e-9

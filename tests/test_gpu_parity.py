@@ -71,6 +71,30 @@ def test_indexer_scores_precision_stress():
     sess.close()
 
 
+@pytest.mark.parametrize("shape", [
+    dict(mtp=3),                                       # N = 192: 64-column chunks
+    dict(mtp=4),                                       # N = 256, the pages' MTP3 (4 ways)
+    dict(mtp=3, idx_heads=32),                         # N = 96: 32-column chunks
+    dict(mtp=4, idx_heads=32, T_per_req=[4096, 700]),  # ragged, a way per 32 columns
+], ids=["3x64", "4x64", "3x32", "4x32_ragged"])
+def test_three_and_four_ways(shape):
+    """More MTP ways than the configs use: scores bit-exact per way, then the
+    whole layer from an empty and from a full pool (FlashOffloading analysis,
+    "decode side (1)": the four-way MTP3 merge into one miss union)."""
+    base = dict(layers=1, batch=2, T=4096, k=256, mla_heads=32, steps=3)
+    base.update(shape)
+    base["C"] = base["mtp"] * base["k"]
+    cfg = W.v32_32k().replace(**base)
+    p = Pair(cfg)
+    for s in range(2):
+        p.run_step(check_scores=(s == 0))
+    p.prime_full(age=4)
+    for _ in range(3):
+        p.run_step()
+    p.check_pool_rows()
+    p.close()
+
+
 # ------------------------------------------------------------------ selection + LRU (a2-a4)
 
 def _planted_ties(rng, shape, k):
@@ -314,10 +338,31 @@ def test_set_state_resumes_from_oracle_state():
                            torch.from_numpy(st.last_used[None].copy()),
                            torch.tensor([st.step], dtype=torch.int32))
     q.compare_state(0)
+    q.check_pool_rows()              # resident rows reloaded from the host copy
     for _ in range(3):
-        q.run_step(check_out=False)
+        q.run_step()
     p.close()
     q.close()
+
+
+@pytest.mark.parametrize("shape", [
+    dict(),                                                     # every slot resident
+    dict(batch=2, T=3072, T_per_req=[3000, 700], k=128, C=1024),  # one request smaller than C
+    dict(batch=2, T=4096, mtp=2, idx_heads=32, k=256, C=512),   # two ways, C = M * k
+], ids=["tiny_full", "ragged_partly_full", "two_ways_tight"])
+def test_full_pool_evictions(shape):
+    """From a full pool every miss evicts a resident token: lists, state and
+    attention stay in step with the oracle, and the pool rows stay equal to the
+    host copy."""
+    cfg = W.tiny().replace(**shape)
+    p = Pair(cfg)
+    p.prime_full(age=5)
+    p.check_pool_rows()
+    for _ in range(6):
+        p.run_step()
+    p.check_pool_rows()
+    assert sum(p.evicted) > 0
+    p.close()
 
 
 def test_set_state_rejects_future_stamps():

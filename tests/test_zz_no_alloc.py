@@ -85,8 +85,12 @@ def test_noalloc_matches_select_manage(shape):
 
 
 def test_noalloc_rejects_oversized_scratch():
-    cfg = dataclasses.replace(W.tiny(), batch=32, mtp=4, idx_heads=32, T=2048, C=512, k=128)
+    # 64 requests x 2 ways: 128 histograms of 16 KiB fill the 2 MiB array alone,
+    # and the victim lists do not fit beside them; the pool itself is valid
+    cfg = dataclasses.replace(W.tiny(), batch=64, mtp=2, idx_heads=32, T=1024, C=256, k=128)
     assert _scratch_need(cfg) > STATIC_SCRATCH_BYTES
+    from host_latent_cache_gb300.session import ess_config_of
+    assert ess.ess_pool_device_bytes(ess_config_of(cfg)) > 0
     ld = W.gen_layer(cfg, 0)
     s = Session(cfg, [ld])
     try:
