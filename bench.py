@@ -69,6 +69,8 @@ def parse():
                          "requests each) on two streams against the same work on one stream")
     ap.add_argument("--append", action="store_true",
                     help="time decode steps that each append one token per request first")
+    ap.add_argument("--policy", default="lru",
+                    help="eviction orders of --miss-sweep, comma-separated: lru,random,score,lim")
     ap.add_argument("--miss-sweep", default=None,
                     help="comma-separated hot-pool sizes C: print the distinct miss rows per "
                          "step of the workload for each instead of the benchmark line")
@@ -318,19 +320,24 @@ def measure_overlap(cfg, ld, n_steps, stream, host_buffers, qs=None, start_state
     qs = qs if qs is not None else W.QueryStream(cfg)
     wts = W.head_weights(cfg, ld.w)
     steps = [qs.next() for _ in range(n_steps)]
-    res, outs = {}, {}
-    for mode in (ess.ESS_MISS_FUSED, ess.ESS_MISS_STAGED):
+    modes = (ess.ESS_MISS_FUSED, ess.ESS_MISS_STAGED)
+    sessions, ins, evs, nms = {}, {}, {}, {}
+    for mode in modes:
         sess = Session(cfg, [ld], miss_mode=mode, host_buffers=host_buffers)
         if start_state is not None:
             sess.set_state(0, start_state)
-        ins = [sess.device_inputs(enc, wts, qm) for (_, enc, qm) in steps]
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in steps]
-        nm = torch.zeros(len(steps), dtype=torch.int64, device=sess.device)
-        torch.cuda.synchronize()
-        # the steps run back to back (no host work between them): the miss
-        # path is slower right after the GPU has been idle
-        for i, (qd, wd, qmd) in enumerate(ins):
-            e = evs[i]
+        sessions[mode] = sess
+        ins[mode] = [sess.device_inputs(enc, wts, qm) for (_, enc, qm) in steps]
+        evs[mode] = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in steps]
+        nms[mode] = torch.zeros(len(steps), dtype=torch.int64, device=sess.device)
+    torch.cuda.synchronize()
+    # the two pools take turns step by step (the host link is shared with other
+    # work on the machine, so a slow phase of it falls on both); the steps run
+    # back to back, with no host work between them
+    for i in range(len(steps)):
+        for mode in modes:
+            sess, e = sessions[mode], evs[mode][i]
+            qd, wd, qmd = ins[mode][i]
             sess.indexer_topk(0, qd, wd, stream)
             e[0].record(stream)
             if mode == ess.ESS_MISS_STAGED:
@@ -338,12 +345,15 @@ def measure_overlap(cfg, ld, n_steps, stream, host_buffers, qs=None, start_state
             e[1].record(stream)
             sess.attention(0, qmd, stream=stream)
             e[2].record(stream)
-            nm[i] = sess.n_miss.sum()
-        torch.cuda.synchronize()
+            nms[mode][i] = sess.n_miss.sum()
+    torch.cuda.synchronize()
+    res, outs = {}, {}
+    for mode in modes:
+        sess = sessions[mode]
         assert sess.poll(stream) == ess.ESS_OK
-        nmh = nm.cpu().tolist()
+        nmh = nms[mode].cpu().tolist()
         res[mode] = [(int(nmh[i]), e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]))
-                     for i, e in enumerate(evs)]
+                     for i, e in enumerate(evs[mode])]
         outs[mode] = sess.out.clone()
         sess.close()
     fz, sg = res[ess.ESS_MISS_FUSED], res[ess.ESS_MISS_STAGED]
@@ -356,7 +366,12 @@ def measure_overlap(cfg, ld, n_steps, stream, host_buffers, qs=None, start_state
     tc = statistics.mean(sg[i][1] for i in rng)
     ts = statistics.mean(sg[i][2] for i in rng)
     tf = statistics.mean(fz[i][2] for i in rng)
+    mc = statistics.median(sg[i][1] for i in rng)
+    ms_ = statistics.median(sg[i][2] for i in rng)
+    mf = statistics.median(fz[i][2] for i in rng)
     out = {"steps": len(rng), "settling_steps_dropped": settle,
+           "median": {"t_copy_us": 1e3 * mc, "t_sfa_us": 1e3 * ms_, "t_fused_us": 1e3 * mf,
+                      "overlap_ratio": (mc + ms_ - mf) / mc if mc > 0 else None},
            "start": "steady state of the timed run" if start_state is not None else "empty pool",
            "miss_rows_per_step": statistics.mean(fz[i][0] for i in rng),
            "t_copy_us": 1e3 * tc, "t_sfa_us": 1e3 * ts, "t_fused_us": 1e3 * tf,
@@ -457,31 +472,35 @@ def measure_link(host_buf, n_host_rows, device, stream, reps=5):
     bad = torch.zeros(1, dtype=torch.int32, device=device)
     g = torch.Generator().manual_seed(4242)
 
-    def timed(fn, nbytes):
+    per_launch = {}
+
+    def timed(fn, nbytes, name):
         fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(reps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        ev[0].record(stream)
+        for i in range(reps):
             fn()
-        e1.record(stream)
+            ev[i + 1].record(stream)
         torch.cuda.synchronize()
-        return nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+        per_launch[name] = [round(ev[i].elapsed_time(ev[i + 1]) * 1e3, 1) for i in range(reps)]
+        return nbytes * reps / (ev[0].elapsed_time(ev[reps]) * 1e-3) / 1e9
 
     res["gather_seq_gbs"] = timed(
         lambda: ess.ess_host_gather(host_buf, n_host_rows, ROW_BYTES, None, n_seq, dst, bad,
-                                    stream), n_seq * ROW_BYTES)
+                                    stream), n_seq * ROW_BYTES, "gather_seq")
     for n in (16384, n_seq):
         rows = torch.randint(0, n_host_rows, (n,), generator=g, dtype=torch.int64).to(device)
         res[f"gather_random_{n}_rows_gbs"] = timed(
             lambda: ess.ess_host_gather(host_buf, n_host_rows, ROW_BYTES, rows, n, dst, bad,
-                                        stream), n * ROW_BYTES)
+                                        stream), n * ROW_BYTES, f"gather_random_{n}")
     hsrc = torch.empty(n_seq * ROW_BYTES, dtype=torch.uint8).pin_memory()
     dflat = dst.view(-1)
     res["copy_engine_h2d_gbs"] = timed(lambda: dflat.copy_(hsrc, non_blocking=True),
-                                       n_seq * ROW_BYTES)
+                                       n_seq * ROW_BYTES, "copy_engine")
     torch.cuda.synchronize()
     assert int(bad.item()) == 0
+    res["per_launch_us"] = per_launch
     res["bytes_per_sequential_read"] = n_seq * ROW_BYTES
     res["peak_gbs"] = max(res["gather_seq_gbs"], res["copy_engine_h2d_gbs"])
     res["peak_source"] = ("measured in this run: the larger of the sequential gather kernel "
@@ -615,7 +634,11 @@ def bench_ours(args, cfg, rank, world, local_rank):
         link = measure_link(sess.host[0], cfg_r.batch * W.t_max_of(cfg_r), sess.device, stream)
 
 
-    # end to end through the public C ABI with host buffers
+    # end to end through the public C ABI with host buffers (two untimed calls
+    # first: the first device access to freshly pinned buffers is slow)
+    for i in range(2):
+        hq, hw, hqm = host_inputs[i]
+        ess.ess_step_host(sess.pool, 0, hq, hw, hqm, out_host, stream)
     torch.cuda.synchronize()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
@@ -705,44 +728,53 @@ def bench_ours(args, cfg, rank, world, local_rank):
     return result, ld
 
 
+POLICIES = {"lru": 0, "random": 1, "score": 2, "lim": 3}   # ESS_EVICT_*
+
+
 def miss_sweep(args, cfg):
     """Distinct miss rows per step (after the first fill) for each hot-pool
-    size C, on the same seeded query stream, through the CUDA path.  The
-    FlashOffloading analysis reports how misses fall as the hot cache grows
-    (section "evaluation", the miss-versus-cache-size figure)."""
+    size C and eviction order, on the same seeded query stream, through the
+    CUDA path.  The FlashOffloading analysis reports how misses fall as the
+    hot cache grows and how little the eviction policy matters (section
+    "evaluation", the decode ablation and Figure 8)."""
     import torch
     from host_latent_cache_gb300 import ess
     from host_latent_cache_gb300.session import Session
     ess.load()
     ld = W.gen_layer(cfg)
     sizes = [int(x) for x in args.miss_sweep.split(",")]
+    policies = args.policy.split(",")
     hb = [ess.HostBuffer(ld.host_latent.shape, np.uint16)]
     hb[0].array[...] = ld.host_latent
     res = {}
-    for C in sizes:
-        c2 = cfg.replace(C=C)
-        sess = Session(c2, [ld], host_buffers=hb)
-        qs = W.QueryStream(c2)
-        wts = W.head_weights(c2, ld.w)
-        stream = torch.cuda.current_stream()
-        for s in range(args.steps):
-            _, enc, qm = qs.next()
-            qd, wd, qmd = sess.device_inputs(enc, wts, qm)
-            if s == 1:
-                torch.cuda.synchronize()
-                sess.stats(0, reset=True)      # the first step fills the empty pool
-            ess.ess_step(sess.pool, 0, qd, wd, qmd, sess.out, stream)
-        torch.cuda.synchronize()
-        assert sess.poll(stream) == ess.ESS_OK
-        st = sess.stats(0, reset=True)
-        res[C] = st.miss_rows / max(1, args.steps - 1) / cfg.batch
-        sess.close()
+    for pol in policies:
+        for C in sizes:
+            c2 = cfg.replace(C=C)
+            sess = Session(c2, [ld], host_buffers=hb)
+            ess.ess_pool_set_eviction(sess.pool, POLICIES[pol], 0x5EED)
+            qs = W.QueryStream(c2)
+            wts = W.head_weights(c2, ld.w)
+            stream = torch.cuda.current_stream()
+            for s in range(args.steps):
+                _, enc, qm = qs.next()
+                qd, wd, qmd = sess.device_inputs(enc, wts, qm)
+                if s == 1:
+                    torch.cuda.synchronize()
+                    sess.stats(0, reset=True)      # the first step fills the empty pool
+                ess.ess_step(sess.pool, 0, qd, wd, qmd, sess.out, stream)
+            torch.cuda.synchronize()
+            assert sess.poll(stream) == ess.ESS_OK
+            st = sess.stats(0, reset=True)
+            res[(pol, C)] = st.miss_rows / max(1, args.steps - 1) / cfg.batch
+            sess.close()
     hb[0].close()
     line = {"miss_sweep": {"workload": cfg.name, "steps_after_first_fill": args.steps - 1,
-                           "C": sizes,
-                           "miss_rows_per_request_step": [res[c] for c in sizes],
-                           "reduction_vs_first": [1.0 - res[c] / res[sizes[0]] if res[sizes[0]]
-                                                  else None for c in sizes]}}
+                           "C": sizes, "policies": policies,
+                           "miss_rows_per_request_step": {
+                               p: [res[(p, c)] for c in sizes] for p in policies},
+                           "reduction_vs_first": {
+                               p: [1.0 - res[(p, c)] / res[(p, sizes[0])] if res[(p, sizes[0])]
+                                   else None for c in sizes] for p in policies}}}
     print(json.dumps(line), flush=True)
     return 0
 

@@ -126,6 +126,26 @@ bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
   return r == CUDA_SUCCESS;
 }
 
+// The LRU order list of a layer from host copies of last_used [B][C] and step
+// [B]: slots by (last_used, slot), in the list that the next step reads.
+cudaError_t write_order(const ess_pool& p, int layer, const std::vector<int32_t>& lu,
+                        const std::vector<int32_t>& sp) {
+  const ess_config& c = p.cfg;
+  const size_t B = c.batch;
+  std::vector<int32_t> ord(c.C);
+  for (size_t b = 0; b < B; ++b) {
+    for (int i = 0; i < c.C; ++i) ord[i] = i;
+    const int32_t* l = lu.data() + b * c.C;
+    std::sort(ord.begin(), ord.end(), [l](int32_t x, int32_t y) {
+      return l[x] != l[y] ? l[x] < l[y] : x < y;
+    });
+    int32_t* dst = p.layers[layer].order + (static_cast<size_t>(sp[b] & 1) * B + b) * c.C;
+    const cudaError_t e = cudaMemcpy(dst, ord.data(), c.C * 4, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_reset(const ess_pool& p, int layer, cudaStream_t st) {
   const ess_config& c = p.cfg;
   const Layer& L = p.layers[layer];
@@ -444,6 +464,19 @@ ess_status ess_step_host(ess_pool* pool, int layer, const void* q_idx_host, cons
   Scratch& r = pool->scr;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t BM = static_cast<size_t>(c.batch) * c.mtp;
+  // mapped pinned buffers: the GPU reads the inputs and writes the output over
+  // the host link itself, inside the step's chain of kernels
+  void *dq = nullptr, *dw = nullptr, *dqm = nullptr, *dout = nullptr;
+  auto alias = [](const void* h, void** d) {
+    return cudaHostGetDevicePointer(d, const_cast<void*>(h), 0) == cudaSuccess;
+  };
+  if (alias(q_idx_host, &dq) && alias(w_host, &dw) && alias(q_mla_host, &dqm) &&
+      alias(out_host, &dout) && aligned16(dq) && aligned16(dw) && aligned16(dqm) &&
+      aligned16(dout)) {
+    if (launch_inputs_in(*pool, dq, dw, dqm, st) != cudaSuccess) return ESS_ERR_CUDA;
+    return ess_step(pool, layer, r.h_qidx, r.h_w, r.h_qmla, static_cast<float*>(dout), stream);
+  }
+  cudaGetLastError();   // a buffer that is not mapped: copy through the staging
   if (cudaMemcpyAsync(r.h_qidx, q_idx_host, BM * c.idx_heads * kKeyRowBytes,
                       cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaMemcpyAsync(r.h_w, w_host, BM * c.idx_heads * 4, cudaMemcpyHostToDevice, st) !=
@@ -524,16 +557,7 @@ ess_status ess_pool_set_state(ess_pool* pool, int layer, const int32_t* cache_sl
   if (slot_token && cudaMemcpy(L.slot_token, slot_token, B * c.C * 4, cudaMemcpyHostToDevice) != cudaSuccess) return ESS_ERR_CUDA;
   if (last_used && cudaMemcpy(L.last_used, last_used, B * c.C * 4, cudaMemcpyHostToDevice) != cudaSuccess) return ESS_ERR_CUDA;
   if (step && cudaMemcpy(L.step, step, B * 4, cudaMemcpyHostToDevice) != cudaSuccess) return ESS_ERR_CUDA;
-  std::vector<int32_t> ord(c.C);
-  for (size_t b = 0; b < B; ++b) {
-    for (int i = 0; i < c.C; ++i) ord[i] = i;
-    const int32_t* l = lu.data() + b * c.C;
-    std::sort(ord.begin(), ord.end(), [l](int32_t x, int32_t y) {
-      return l[x] != l[y] ? l[x] < l[y] : x < y;
-    });
-    int32_t* dst = L.order + (static_cast<size_t>(sp[b] & 1) * B + b) * c.C;
-    if (cudaMemcpy(dst, ord.data(), c.C * 4, cudaMemcpyHostToDevice) != cudaSuccess) return ESS_ERR_CUDA;
-  }
+  if (write_order(*pool, layer, lu, sp) != cudaSuccess) return ESS_ERR_CUDA;
   // the rows of the resident tokens come from the authoritative host copy
   if (L.bound) {
     if (launch_refill(*pool, layer, nullptr) != cudaSuccess) return ESS_ERR_CUDA;
@@ -556,6 +580,26 @@ ess_status ess_host_gather(const void* host_rows, int64_t n_host_rows, int32_t r
   }
   return cuda_status(launch_host_gather(dev_alias, rows, n_rows, n_host_rows, row_bytes, dst,
                                         bad_row, static_cast<cudaStream_t>(stream)));
+}
+
+ess_status ess_pool_set_eviction(ess_pool* pool, int32_t policy, uint64_t seed) {
+  if (!pool || policy < ESS_EVICT_LRU || policy > ESS_EVICT_LIM) return ESS_ERR_INVALID_ARG;
+  const ess_config& c = pool->cfg;
+  if (policy == ESS_EVICT_LRU && pool->evict_policy != ESS_EVICT_LRU) {
+    // the LRU list was not kept under the other order: rebuild it from the stamps
+    if (cudaDeviceSynchronize() != cudaSuccess) return ESS_ERR_CUDA;
+    std::vector<int32_t> lu(static_cast<size_t>(c.batch) * c.C), sp(c.batch);
+    for (int l = 0; l < c.n_layers; ++l) {
+      const Layer& L = pool->layers[l];
+      if (cudaMemcpy(lu.data(), L.last_used, lu.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+          cudaMemcpy(sp.data(), L.step, sp.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+          write_order(*pool, l, lu, sp) != cudaSuccess)
+        return ESS_ERR_CUDA;
+    }
+  }
+  pool->evict_policy = policy;
+  pool->evict_seed = seed;
+  return ESS_OK;
 }
 
 ess_status ess_pool_get_rows(ess_pool* pool, int layer, void* rows_host) {

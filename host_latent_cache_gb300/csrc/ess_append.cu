@@ -133,4 +133,70 @@ cudaError_t launch_append(const ess_pool& p, int layer, const void* latent, cons
   return e;
 }
 
+// ---------------------------------------------------------------------------
+// Step inputs straight from mapped pinned host memory: three segments of
+// 16-byte units (indexer queries, head weights, MLA queries) copied into the
+// pool's staging by the GPU's own threads.  The host reads are issued before
+// the wait for the previous grid (nothing on the device writes the caller's
+// host inputs), so they overlap that grid's tail; the staging is written
+// after it (the previous step's attention reads the staged MLA queries).
+namespace {
+
+struct InSeg {
+  const uint4* src;
+  uint4* dst;
+  long long n;   // 16-byte units
+};
+
+constexpr int kInPerThread = 2;
+
+__global__ void __launch_bounds__(256) inputs_in_kernel(const InSeg s0, const InSeg s1,
+                                                        const InSeg s2) {
+  const long long i0 =
+      (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * kInPerThread;
+  uint4 v[kInPerThread];
+  uint4* d[kInPerThread];
+#pragma unroll
+  for (int u = 0; u < kInPerThread; ++u) {
+    long long i = i0 + u;
+    d[u] = nullptr;
+    if (i < s0.n) {
+      v[u] = s0.src[i];
+      d[u] = s0.dst + i;
+    } else if ((i -= s0.n) < s1.n) {
+      v[u] = s1.src[i];
+      d[u] = s1.dst + i;
+    } else if ((i -= s1.n) < s2.n) {
+      v[u] = s2.src[i];
+      d[u] = s2.dst + i;
+    }
+  }
+  pdl_wait_previous();
+  pdl_launch_dependents();
+#pragma unroll
+  for (int u = 0; u < kInPerThread; ++u)
+    if (d[u]) *d[u] = v[u];
+}
+
+}  // namespace
+
+cudaError_t launch_inputs_in(const ess_pool& p, const void* q_idx_dev, const void* w_dev,
+                             const void* q_mla_dev, cudaStream_t st) {
+  const ess_config& c = p.cfg;
+  const long long BM = static_cast<long long>(c.batch) * c.mtp;
+  InSeg s0{static_cast<const uint4*>(q_idx_dev), reinterpret_cast<uint4*>(p.scr.h_qidx),
+           BM * c.idx_heads * kKeyRowBytes / 16};
+  InSeg s1{static_cast<const uint4*>(w_dev), reinterpret_cast<uint4*>(p.scr.h_w),
+           BM * c.idx_heads * 4 / 16};
+  InSeg s2{static_cast<const uint4*>(q_mla_dev), reinterpret_cast<uint4*>(p.scr.h_qmla),
+           BM * c.mla_heads * kRowBytes / 16};
+  const long long n = s0.n + s1.n + s2.n;
+  const long long per_cta = 256LL * kInPerThread;
+  const cudaError_t e =
+      launch_pdl(inputs_in_kernel, dim3(static_cast<unsigned>((n + per_cta - 1) / per_cta)),
+                 dim3(256), 0, st, s0, s1, s2);
+  if (e == cudaSuccess) count_launch(p);
+  return e;
+}
+
 }  // namespace ess

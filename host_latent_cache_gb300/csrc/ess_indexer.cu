@@ -47,12 +47,29 @@ struct IdxArgs {
 };
 
 constexpr uint32_t kTileBytes = kIdxTile * kKeyRowBytes;  // 16 KB
+constexpr int kMaxAcc = 8;   // TMEM accumulators in flight (A * N <= 512 columns)
 
-__device__ __forceinline__ int find_request(const int32_t* tile_off, int B, int g) {
-  int b = 0;
-  while (b + 1 < B && g >= tile_off[b + 1]) ++b;
-  return b;
-}
+// Walks a CTA's tiles in order over the concatenated requests: request b
+// owns tiles [lo, hi); the tile prefix is read only when the request changes.
+struct TileCursor {
+  const int32_t* off;
+  int B, b, lo, hi;
+  __device__ __forceinline__ void start(const int32_t* o, int nb, int g) {
+    off = o;
+    B = nb;
+    b = 0;
+    lo = 0;
+    hi = nb > 1 ? o[1] : 0x7fffffff;
+    advance(g);
+  }
+  __device__ __forceinline__ void advance(int g) {
+    while (b + 1 < B && g >= hi) {
+      ++b;
+      lo = hi;
+      hi = b + 1 < B ? off[b + 1] : 0x7fffffff;
+    }
+  }
+};
 
 template <bool FP8>
 __global__ void __launch_bounds__(kIdxThreads, 1)
@@ -73,8 +90,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   uint64_t* full = bars;
   uint64_t* empty = full + S;
   uint64_t* accf = empty + S;
-  uint64_t* acce = accf + 4;
-  uint64_t* qfull = acce + 4;
+  uint64_t* acce = accf + kMaxAcc;
+  uint64_t* qfull = acce + kMaxAcc;
   uint64_t* qempty = qfull + 2;
   uint64_t* epdone = qempty + 2;      // every epilogue thread has counted its tiles
   uint64_t* fldone = epdone + 2;      // the histogram is flushed and clear again
@@ -96,7 +113,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), 1);
     }
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(smem_u32(&accf[i]), 1);
       mbar_init(smem_u32(&acce[i]), 128);
     }
@@ -133,13 +150,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   int n_early = 0;
   if (warp == 0 && a.early) {
     if (lane == 0) {
-      int b = find_request(a.tile_off, a.B, g0);
+      TileCursor tc;
+      tc.start(a.tile_off, a.B, g0);
       for (int g = g0; g < g1 && n_early < S; ++g, ++n_early) {
-        while (b + 1 < a.B && g >= a.tile_off[b + 1]) ++b;
-        const int j = g - a.tile_off[b];
+        tc.advance(g);
         mbar_arrive_expect_tx(smem_u32(&full[n_early]), kTileBytes);
         tma_load_2d(smem_u32(kst + n_early * kTileBytes), &kmap, smem_u32(&full[n_early]), 0,
-                    b * a.T + j * kIdxTile);
+                    tc.b * a.T + (g - tc.lo) * kIdxTile);
       }
     }
     n_early = __shfl_sync(0xffffffffu, n_early, 0);
@@ -149,12 +166,14 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------ producer
-    int b = find_request(a.tile_off, a.B, g0);
+    TileCursor tc;
+    tc.start(a.tile_off, a.B, g0);
     int cur_b = -1, seg = -1, it = 0;
     bool ok = true;
     for (int g = g0; g < g1 && ok; ++g, ++it) {
-      while (b + 1 < a.B && g >= a.tile_off[b + 1]) ++b;
-      const int j = g - a.tile_off[b];
+      tc.advance(g);
+      const int b = tc.b;
+      const int j = g - tc.lo;
       if (b != cur_b) {
         ++seg;
         const int qb = seg & 1;
@@ -209,10 +228,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = FP8 ? make_idesc(kFmtE4M3, kFmtE4M3, 0, NP, 128)
                                  : make_idesc(kFmtBF16, kFmtBF16, 0, NP, 128);
-      int b = find_request(a.tile_off, a.B, g0);
+      TileCursor tc;
+      tc.start(a.tile_off, a.B, g0);
       int cur_b = -1, seg = -1, it = 0;
       for (int g = g0; g < g1; ++g, ++it) {
-        while (b + 1 < a.B && g >= a.tile_off[b + 1]) ++b;
+        tc.advance(g);
+        const int b = tc.b;
         if (b != cur_b) {
           if (seg >= 0) umma_commit(smem_u32(&qempty[seg & 1]));
           ++seg;
@@ -248,15 +269,17 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     const int quad = warp & 3;               // TMEM lanes 32*quad .. +31
     const int row = quad * 32 + lane;        // token row of the tile
     const int te = tid - 64;                 // 0..255
-    int b = find_request(a.tile_off, a.B, g0);
+    TileCursor tc;
+    tc.start(a.tile_off, a.B, g0);
     int cur_b = -1, seg = -1, it = 0;
     int Tcur = 0;
     bool ok = true;
     // 64-column TMEM loads when no chunk straddles two ways
     const bool wide = (NP % 64 == 0) && (a.M == 1 || a.HI % 64 == 0);
     for (int g = g0; g < g1 && ok; ++g, ++it) {
-      while (b + 1 < a.B && g >= a.tile_off[b + 1]) ++b;
-      const int j = g - a.tile_off[b];
+      tc.advance(g);
+      const int b = tc.b;
+      const int j = g - tc.lo;
       if (b != cur_b) {
         ++seg;
         if (!mbar_wait(smem_u32(&qfull[seg & 1]), (seg >> 1) & 1, abort_flag)) break;
@@ -352,7 +375,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       }
       // end of this request's run of tiles: release the query buffer and
       // publish the histogram once every epilogue thread has counted
-      const bool last = (g + 1 == g1) || (g + 1 >= a.tile_off[b + 1]);
+      const bool last = (g + 1 == g1) || (g + 1 >= tc.hi);
       if (last) {
         mbar_arrive(smem_u32(&qempty[seg & 1]));
         if (HB) {
@@ -384,7 +407,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
 size_t indexer_smem_bytes(int S, int NP, int HB) {
   return 1024 + static_cast<size_t>(S) * kTileBytes + 2u * NP * 128 + 2u * NP * 4 + HB * 4u +
-         (2 * S + 8 + 8) * 8 + 16;
+         (2 * S + 2 * kMaxAcc + 8) * 8 + 16;
 }
 
 // Largest key ring (at most kIdxMaxStages) that fits one CTA beside the
@@ -424,7 +447,7 @@ cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, cons
   a.NP = ((c.mtp * c.idx_heads + 31) / 32) * 32;
   a.T = c.max_T;
   a.total_tiles = L.total_tiles;
-  a.A = 512 / a.NP < 4 ? 512 / a.NP : 4;
+  a.A = 512 / a.NP < kMaxAcc ? 512 / a.NP : kMaxAcc;
   const int HB = with_hist ? c.mtp * kHistBins : 0;
   a.S = indexer_stages(a.NP, HB);
   a.early = L.append_pending ? 0 : 1;

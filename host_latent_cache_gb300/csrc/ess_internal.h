@@ -21,7 +21,11 @@ constexpr int kKeyRowBytes = 128;     // one indexer key row
 
 constexpr int kIdxThreads = 320;      // 10 warps: TMA, MMA, 2 groups of 4 epilogue warps
 constexpr int kHistBins = 4096;       // score histogram on the top 12 bits of the ordered key
-constexpr int kIdxMaxStages = 12;     // key-tile ring: as many 16 KB stages as fit, up to 12
+// key-tile ring: as many 16 KB stages as fit one CTA, up to kIdxMaxStages
+#ifndef ESS_IDX_MAX_STAGES
+#define ESS_IDX_MAX_STAGES 6
+#endif
+constexpr int kIdxMaxStages = ESS_IDX_MAX_STAGES;
 constexpr int kIdxMinStages = 4;
 constexpr int kIdxTile = 128;         // tokens per tile (MMA M)
 
@@ -109,6 +113,8 @@ struct ess_pool {
   ess::Layout lay;
   ess::Layer* layers = nullptr;
   ess::Scratch scr;
+  int32_t evict_policy = ESS_EVICT_LRU;  // victim order of the decode kernels
+  unsigned long long evict_seed = 0;     // key of the Random order
   long long launches = 0;          // kernels launched by this pool's calls
   long long* n_launch = nullptr;   // -> launches (copies of the handle count into it)
 };
@@ -184,6 +190,10 @@ cudaError_t launch_reset(const ess_pool& p, int layer, cudaStream_t st);
 cudaError_t launch_host_gather(const void* host_dev, const int64_t* rows, int64_t n_rows,
                                int64_t n_host_rows, int row_bytes, void* dst, int* status,
                                cudaStream_t st);
+// the step inputs of ess_step_host from device aliases of mapped pinned host
+// buffers into the pool's staging (one kernel, a programmatic dependent)
+cudaError_t launch_inputs_in(const ess_pool& p, const void* q_idx_dev, const void* w_dev,
+                             const void* q_mla_dev, cudaStream_t st);
 // reload the pool rows of every resident token from the host copy
 cudaError_t launch_refill(const ess_pool& p, int layer, cudaStream_t st);
 cudaError_t launch_append(const ess_pool& p, int layer, const void* latent, const void* key,

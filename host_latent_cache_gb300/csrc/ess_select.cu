@@ -39,6 +39,7 @@
 // reads (the emitted lists, the miss union and its victims), and
 // lru_finish_kernel, which only the next step depends on, rewrites the state
 // and closes the next LRU list while the attention kernel runs.
+#include <algorithm>
 #include <mutex>
 
 #include "ess_device.cuh"
@@ -74,6 +75,9 @@ struct SelArgs {
   long long* stats;           // [kStatFields]
   int* status;
   int B, M, k, T, C;
+  int policy;                 // ESS_EVICT_*: LRU keeps the order list; the others
+                              // leave the victims to victim_kernel
+  unsigned long long seed;    // key of the Random victim order
   int n_local;                // tokens per CTA (multiple of 4)
   int c_local;                // slots / order positions per CTA
   int resident;               // scores staged in shared memory
@@ -347,7 +351,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   // this CTA's positions of the current LRU list (read after the hits are stamped)
   const int step0 = a.step[b];
   const int p0 = static_cast<int>(rank) * a.c_local;
-  int cl = a.C - p0;
+  const bool lru = a.policy == ESS_EVICT_LRU;
+  int cl = lru ? a.C - p0 : 0;   // other policies do not use the LRU list
   cl = cl < 0 ? 0 : (cl > a.c_local ? a.c_local : cl);
   const int32_t* ocur = a.order + (static_cast<size_t>(step0 & 1) * a.B + b) * a.C;
   int32_t* onxt = a.order + (static_cast<size_t>((step0 & 1) ^ 1) * a.B + b) * a.C;
@@ -866,7 +871,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   __syncthreads();
   {
     // unstamped slots in LRU order: the first |Miss| are the victims, the rest
-    // open the next list (each warp places its own contiguous positions)
+    // open the next list (each warp places its own contiguous positions);
+    // with another policy cl is 0 and victim_kernel lists the victims
     int wcnt = 0;
     for (int base = clo; base < chi; base += 32) {
       const int i = base + lane;
@@ -890,7 +896,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   }
   __syncthreads();
   cluster_sync();  // [S5] victims listed; no shared memory is read remotely after this
-  if (n_miss_total > 0) {
+  if (n_miss_total > 0 && lru) {
     // the i-th miss goes to the i-th victim (the state rewrite and the rest of
     // the next LRU list are left to lru_finish_kernel)
     const int per = (n_miss_total + CL - 1) / CL;
@@ -919,9 +925,14 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       const int ph = ordered_pos(fh ? 1 : 0, runh, sh, parity);
       if (fm && pm < a.k) {
         const int mi = -2 - s;
-        const int ns = (mi >= 0 && mi < n_miss_total) ? a.vlist[static_cast<size_t>(b) * MK + mi] : 0;
         a.topk_idx[wo + pm] = t;
-        a.topk_slot[wo + pm] = ~ns;
+        if (lru) {
+          const int ns =
+              (mi >= 0 && mi < n_miss_total) ? a.vlist[static_cast<size_t>(b) * MK + mi] : 0;
+          a.topk_slot[wo + pm] = ~ns;
+        } else {
+          a.topk_slot[wo + pm] = -2 - mi;   // its miss index; victim_kernel puts ~slot here
+        }
       }
       if (fh && ph < a.k) {
         a.topk_idx[wo + ph] = t;
@@ -984,7 +995,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   const unsigned lt = lanemask_lt();
   const int step_b = a.step[b];
   const int p0 = static_cast<int>(rank) * a.c_local;
-  int cl = a.C - p0;
+  // the LRU list is kept only under the LRU policy (cl = 0 skips its upkeep)
+  int cl = a.policy == ESS_EVICT_LRU ? a.C - p0 : 0;
   cl = cl < 0 ? 0 : (cl > a.c_local ? a.c_local : cl);
   int32_t* onxt = a.order + (static_cast<size_t>((step_b & 1) ^ 1) * a.B + b) * a.C;
   int n_miss_total = a.n_miss[b];
@@ -1078,6 +1090,292 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   if (rank == 0 && tid == 0) a.step[b] = step_b + 1;
 }
 
+// (a4) victims under the Random, Score and LIM orders ([FO] "evaluation",
+// the decode ablation: the same access sequence with only the eviction policy
+// changed).  One CTA per request, after the selection kernel has stamped the
+// hits and built the miss union.  Candidates are the slots whose token is not
+// in the union: empty slots first in slot order, then the resident ones by
+// the policy's key (Score: the token's score this step, the maximum over the
+// ways; Random: a SplitMix64 draw keyed by (seed, request, step) and the slot;
+// LIM: none, i.e. slot order), ties to the lower slot.  The first |Miss| are
+// the victims, in that order: an exact radix select finds them, a bitonic
+// sort orders them.  Then the paired slots go to miss_slot and into the
+// misses' topk_slot entries (~slot), which the selection left as miss indices.
+constexpr int kVicThreads = 1024;
+
+__device__ __forceinline__ unsigned long long mix64(unsigned long long z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+  return z ^ (z >> 31);
+}
+
+struct VicShared {
+  unsigned int hist[256];
+  int scan[kVicThreads / 32];
+  int need;
+  unsigned long long prefix, mask;
+};
+
+// Shared memory of victim_kernel: the sort buffer (ns entries of key + slot),
+// then, when they fit, each slot's class (1 byte) and, for Score, its 32-bit
+// key; without them the kernel reads them again from global memory.
+struct VicSmem {
+  int ns;
+  bool cls_cached, key_cached;
+  size_t bytes;
+};
+
+VicSmem vic_smem(const ess_config& c) {
+  VicSmem v;
+  const int need = std::min(c.mtp * c.k, c.C);
+  v.ns = 1;
+  while (v.ns < need) v.ns <<= 1;
+  const size_t sort = static_cast<size_t>(v.ns) * 12;
+  const size_t budget = kMaxSmemPerCta - sizeof(VicShared) - 1024;
+  const size_t cls = (static_cast<size_t>(c.C) + 15) / 16 * 16;
+  const size_t key = static_cast<size_t>(c.C) * 4;
+  v.cls_cached = sort + cls <= budget;
+  v.key_cached = v.cls_cached && sort + cls + key <= budget;
+  v.bytes = sort + (v.cls_cached ? cls : 0) + (v.key_cached ? key : 0);
+  return v;
+}
+
+__global__ void __launch_bounds__(kVicThreads, 1)
+    victim_kernel(const SelArgs a, int ns, int cls_cached, int key_cached) {
+  pdl_wait_previous();
+  pdl_launch_dependents();
+  extern __shared__ __align__(16) uint8_t dsm[];
+  __shared__ VicShared sh;
+  unsigned long long* skey = reinterpret_cast<unsigned long long*>(dsm);   // [ns]
+  int* sslot = reinterpret_cast<int*>(skey + ns);                          // [ns]
+  uint8_t* scls = reinterpret_cast<uint8_t*>(sslot + ns);                  // [C] if cached
+  uint32_t* skey32 = reinterpret_cast<uint32_t*>(scls + (a.C + 15) / 16 * 16);  // [C] if cached
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x;
+  const int M = a.M, C = a.C, MK = a.M * a.k;
+  const size_t bC = static_cast<size_t>(b) * C;
+  const int step_b = a.step[b];
+  int n = a.n_miss[b];
+  if (n < 0 || n > MK || n > C) n = 0;
+  int32_t* vl = a.vlist + static_cast<size_t>(b) * MK;
+  const bool score = a.policy == ESS_EVICT_SCORE, random = a.policy == ESS_EVICT_RANDOM;
+  // slots [s0, s1) belong to this thread, in slot order across threads
+  const int per = (C + kVicThreads - 1) / kVicThreads;
+  const int s0 = tid * per < C ? tid * per : C;
+  const int s1 = s0 + per < C ? s0 + per : C;
+  const unsigned long long rkey =
+      mix64((mix64((a.seed ^ static_cast<unsigned long long>(b)) + 0x9E3779B97F4A7C15ULL) ^
+             static_cast<unsigned long long>(step_b)) + 0x9E3779B97F4A7C15ULL);
+  // class of a slot from global memory: 0 not a candidate (its token is in the
+  // union: stamped this step), 1 empty, 2 resident; and a resident's key
+  auto classify_global = [&](int sl, unsigned long long& key) -> int {
+    if (a.last_used[bC + sl] == step_b) return 0;
+    const int t = a.slot_token[bC + sl];
+    if (t < 0) return 1;
+    if (score) {
+      float best = a.scores[(static_cast<size_t>(b) * M) * a.T + t];
+      for (int m = 1; m < M; ++m)
+        best = fmaxf(best, a.scores[(static_cast<size_t>(b) * M + m) * a.T + t]);
+      key = float_key(best + 0.0f);
+    } else if (random) {
+      key = mix64(rkey + static_cast<unsigned long long>(sl + 1) * 0x9E3779B97F4A7C15ULL);
+    } else {
+      key = 0;   // LIM: slot order
+    }
+    return 2;
+  };
+  auto classify = [&](int sl, unsigned long long& key) -> int {
+    if (!cls_cached) return classify_global(sl, key);
+    const int c = scls[sl];
+    if (c == 2) {
+      if (score) {
+        if (key_cached) key = skey32[sl];
+        else classify_global(sl, key);
+      } else if (random) {
+        key = mix64(rkey + static_cast<unsigned long long>(sl + 1) * 0x9E3779B97F4A7C15ULL);
+      } else {
+        key = 0;
+      }
+    }
+    return c;
+  };
+  // exclusive prefix over threads of v (block-wide), total in tot
+  auto bscan = [&](int v, int& tot) -> int {
+    int x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    __syncthreads();
+    if (lane == 31) sh.scan[warp] = x;
+    __syncthreads();
+    int pre = 0, t = 0;
+    for (int i = 0; i < kVicThreads / 32; ++i) {
+      const int u = sh.scan[i];
+      pre += i < warp ? u : 0;
+      t += u;
+    }
+    tot = t;
+    return pre + x - v;
+  };
+  // one pass from global memory: classes (and Score keys) into shared memory,
+  // eight slots' loads in flight at a time; and the count of empty slots
+  int ne = 0;
+  for (int g = s0; g < s1; g += 8) {
+    int lu[8], tk[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      lu[u] = g + u < s1 ? a.last_used[bC + g + u] : step_b;
+      tk[u] = g + u < s1 ? a.slot_token[bC + g + u] : -1;
+    }
+    float best[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      best[u] = 0.0f;
+      if (score && lu[u] != step_b && tk[u] >= 0) {
+        best[u] = a.scores[(static_cast<size_t>(b) * M) * a.T + tk[u]];
+        for (int m = 1; m < M; ++m)
+          best[u] = fmaxf(best[u], a.scores[(static_cast<size_t>(b) * M + m) * a.T + tk[u]]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (g + u >= s1) break;
+      const int c = lu[u] == step_b ? 0 : (tk[u] < 0 ? 1 : 2);
+      ne += c == 1 ? 1 : 0;
+      if (cls_cached) scls[g + u] = static_cast<uint8_t>(c);
+      if (key_cached) skey32[g + u] = float_key(best[u] + 0.0f);
+    }
+  }
+  __syncthreads();
+  // empty candidates come first, in slot order
+  int E;
+  int pe = bscan(ne, E);
+  for (int sl = s0; sl < s1 && pe < n; ++sl) {
+    unsigned long long k;
+    if (classify(sl, k) == 1) vl[pe++] = sl;
+  }
+  const int R = n > E ? n - E : 0;   // resident victims
+  if (R > 0) {
+    // exact radix select, smallest first, 8-bit digits from the top of the key
+    const int nbits = random ? 64 : (score ? 32 : 0);
+    if (tid == 0) {
+      sh.prefix = 0;
+      sh.mask = 0;
+      sh.need = R;
+    }
+    __syncthreads();   // (LIM has no pass that would synchronise before the reads below)
+    for (int hi = nbits; hi > 0; hi -= 8) {
+      const int lo = hi - 8;
+      for (int i = tid; i < 256; i += kVicThreads) sh.hist[i] = 0;
+      __syncthreads();
+      const unsigned long long pre = sh.prefix, msk = sh.mask;
+      for (int sl = s0; sl < s1; ++sl) {
+        unsigned long long k = 0;
+        if (classify(sl, k) == 2 && (k & msk) == pre) atomicAdd(&sh.hist[(k >> lo) & 255u], 1u);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane l owns bins 8l..8l+7 (ascending)
+        int c8[8], s8 = 0;
+        for (int j = 0; j < 8; ++j) {
+          c8[j] = static_cast<int>(sh.hist[8 * lane + j]);
+          s8 += c8[j];
+        }
+        int incl = s8;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int need = sh.need;
+        const int excl = incl - s8;
+        if (excl < need && need <= incl) {
+          int acc = excl, j = 0;
+          for (; j < 7; ++j) {
+            if (acc + c8[j] >= need) break;
+            acc += c8[j];
+          }
+          sh.prefix = pre | (static_cast<unsigned long long>(8 * lane + j) << lo);
+          sh.mask = msk | (255ULL << lo);
+          sh.need = need - acc;
+        }
+      }
+      __syncthreads();
+    }
+    // residents below the threshold key, and the lowest-slot equal ones
+    const unsigned long long thr = sh.prefix;
+    const int take_eq = sh.need;
+    int nlt = 0, neq = 0;
+    for (int sl = s0; sl < s1; ++sl) {
+      unsigned long long k = 0;
+      if (classify(sl, k) == 2) {
+        nlt += k < thr ? 1 : 0;
+        neq += k == thr ? 1 : 0;
+      }
+    }
+    int tot_lt, tot_eq;
+    int plt = bscan(nlt, tot_lt);
+    int peq = bscan(neq, tot_eq);
+    for (int sl = s0; sl < s1; ++sl) {
+      unsigned long long k = 0;
+      if (classify(sl, k) != 2) continue;
+      int pos = -1;
+      if (k < thr) pos = plt++;
+      else if (k == thr && peq < take_eq) pos = tot_lt + peq++;
+      if (pos >= 0 && pos < ns) {
+        skey[pos] = k;
+        sslot[pos] = sl;
+      }
+    }
+    if (tid == 0 && (tot_lt + take_eq != R || R > ns)) set_status(a.status, ESS_ERR_DEVICE_CHECK);
+    // bitonic sort of the R victims by (key, slot), padded to a power of two
+    int N = 1;
+    while (N < R) N <<= 1;
+    if (N > ns) N = ns;
+    for (int i = R + tid; i < N; i += kVicThreads) {
+      skey[i] = ~0ULL;
+      sslot[i] = 0x7fffffff;
+    }
+    __syncthreads();
+    for (int kk = 2; kk <= N; kk <<= 1) {
+      for (int j = kk >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < N; i += kVicThreads) {
+          const int l = i ^ j;
+          if (l > i) {
+            const bool up = (i & kk) == 0;
+            const unsigned long long ki = skey[i], kl = skey[l];
+            const int si = sslot[i], sl2 = sslot[l];
+            const bool gt = ki > kl || (ki == kl && si > sl2);
+            if (gt == up) {
+              skey[i] = kl;
+              skey[l] = ki;
+              sslot[i] = sl2;
+              sslot[l] = si;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = tid; i < R && i < N; i += kVicThreads) vl[E + i] = sslot[i];
+  }
+  __syncthreads();
+  // the paired slots: copy triples and the misses' slot entries
+  for (int i = tid; i < n; i += kVicThreads) a.miss_slot[static_cast<size_t>(b) * MK + i] = vl[i];
+  for (int m = 0; m < M; ++m) {
+    const size_t wo = (static_cast<size_t>(b) * M + m) * a.k;
+    const int nm = a.n_miss_way[b * M + m];
+    for (int e = tid; e < nm && e < a.k; e += kVicThreads) {
+      const int mi = -2 - a.topk_slot[wo + e];
+      if (mi < 0 || mi >= n) {
+        set_status(a.status, ESS_ERR_DEVICE_CHECK);
+        continue;
+      }
+      a.topk_slot[wo + e] = ~vl[mi];
+    }
+  }
+}
+
 __global__ void order_reset_kernel(int32_t* order, int n_per_list, int C) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < 2 * n_per_list) order[i] = (i % n_per_list) % C;
@@ -1161,6 +1459,8 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
   a.k = c.k;
   a.T = c.max_T;
   a.C = c.C;
+  a.policy = p.evict_policy;
+  a.seed = p.evict_seed;
   const SelSizes z = sel_sizes(c, L.T_hmax);
   a.n_local = z.nl;
   a.c_local = z.c_local;
@@ -1183,6 +1483,16 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
   e = launch_pdl(kern, dim3(c.batch * CL), dim3(NT), smem, st, a);
   if (e != cudaSuccess) return e;
   count_launch(p);
+  if (a.policy != ESS_EVICT_LRU) {
+    const VicSmem v = vic_smem(c);
+    e = cudaFuncSetAttribute(victim_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(v.bytes));
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(victim_kernel, dim3(c.batch), dim3(kVicThreads), v.bytes, st, a, v.ns,
+                   v.cls_cached ? 1 : 0, v.key_cached ? 1 : 0);
+    if (e != cudaSuccess) return e;
+    count_launch(p);
+  }
   const size_t smem_b = (static_cast<size_t>(a.c_local) + 15) / 16 * 16;
   e = cudaFuncSetAttribute(lru_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_b));

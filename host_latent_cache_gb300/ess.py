@@ -41,7 +41,7 @@ EXPORTS = (
     "ess_step_profiled", "ess_step_host",
     "ess_pipeline_step", "ess_pool_get_state", "ess_pool_set_state", "ess_pool_get_rows",
     "ess_pool_read_stats", "ess_pool_poll", "ess_pool_kernel_launches", "ess_prefill_plan",
-    "ess_compact_rows", "ess_replay_misses", "ess_host_gather",
+    "ess_compact_rows", "ess_replay_misses", "ess_host_gather", "ess_pool_set_eviction",
 )
 
 
@@ -112,6 +112,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "ess_compact_rows": [P, ctypes.c_int64, P],
         "ess_replay_misses": [I, I, P, P, P, I, I, I, ctypes.c_uint64, ctypes.c_int64, P, P],
         "ess_host_gather": [P, ctypes.c_int64, I, P, ctypes.c_int64, P, P, P],
+        "ess_pool_set_eviction": [P, I, ctypes.c_uint64],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -368,3 +369,9 @@ def ess_host_gather(host_rows, n_host_rows: int, row_bytes: int, rows, n_rows: i
     check(load().ess_host_gather(_p(host_rows), int(n_host_rows), int(row_bytes), _p(rows),
                                  int(n_rows), _p(dst), _p(bad_row), _stream(stream)),
           "ess_host_gather")
+
+
+def ess_pool_set_eviction(pool, policy: int, seed: int = 0) -> None:
+    """Victim order of the decode kernels (ESS_EVICT_*)."""
+    check(load().ess_pool_set_eviction(pool, int(policy), seed & ((1 << 64) - 1)),
+          "ess_pool_set_eviction")

@@ -291,9 +291,16 @@ ess_status ess_step_profiled(ess_pool* pool, int layer, const void* q_idx, const
                              const void* q_mla, float* out, ess_stream_t stream,
                              void* const* events);
 
-/* ess_step with HOST inputs and output: the inputs are copied to device
- * staging, the step runs, and out is copied back, all on stream (pass pinned
- * host buffers for asynchronous copies).  Same layouts as ess_step. */
+/* ess_step with HOST inputs and output.  Same layouts as ess_step.
+ * When every buffer is pinned host memory mapped into the device address space
+ * (ess_host_alloc, or cudaHostAlloc / cudaHostRegister on a system with unified
+ * addressing), one more kernel at the head of the step reads the inputs over
+ * the host link into device staging, and the merge kernel writes out_host
+ * directly: no copy engine and no extra synchronisation inside the step.
+ * Otherwise the inputs are copied to the staging and out back with
+ * cudaMemcpyAsync on stream.  Either way the call is asynchronous on stream:
+ * the caller keeps the inputs unchanged, and reads out_host, only after the
+ * stream has passed the call. */
 ess_status ess_step_host(ess_pool* pool, int layer, const void* q_idx_host,
                          const float* w_host, const void* q_mla_host, float* out_host,
                          ess_stream_t stream);
@@ -360,10 +367,26 @@ ess_status ess_pool_kernel_launches(const ess_pool* pool, int64_t* count);
 /* Victim orders of ess_replay_misses. */
 enum { ESS_EVICT_LRU = 0, ESS_EVICT_RANDOM = 1, ESS_EVICT_SCORE = 2, ESS_EVICT_LIM = 3 };
 
+/* Victim order of the decode kernels for every layer of the pool (default
+ * LRU).  The pages' decode ablation compares Random, LRU, Score and LIM on the
+ * same access sequence ([FO] "evaluation", Figure 8); this makes the GPU path
+ * run each of them.  Candidates are the slots whose token is not in the
+ * step's miss union: empty slots first in slot order, then the resident ones
+ * by last use (LRU), by a SplitMix64 draw keyed by (seed, request index b,
+ * the layer's step counter) and the slot (Random), by the token's score this
+ * step, the maximum over the ways (Score), or in slot order (LIM); ties go to
+ * the lower slot, and the i-th miss (ascending token) takes the i-th
+ * candidate, as in ess_replay_misses.  Orders other than LRU add one kernel
+ * per selection.  Synchronous; switching back to LRU rebuilds its order from
+ * last_used.
+ * Errors: ESS_ERR_INVALID_ARG for an unknown policy. */
+ess_status ess_pool_set_eviction(ess_pool* pool, int32_t policy, uint64_t seed);
+
 /* Replay one request's trace of selections with an eviction policy and count
  * its misses ([FO] "evaluation": the decode ablation's offline simulator and
  * Figure 8, which replays the same top-k trace with Random, LRU, Score and
- * LIM eviction).  Host code only; the decode kernels always use LRU.
+ * LIM eviction).  Host code only; ess_pool_set_eviction runs the same
+ * orders in the decode kernels.
  *   offsets, tokens  the selections in CSR form: way m of step s selected
  *                    tokens[offsets[s*n_ways+m] .. offsets[s*n_ways+m+1])
  *   scores           host float [n_steps][n_ways][T], the ways' scores of every

@@ -220,6 +220,49 @@ def test_ess_step_matches_separate_calls():
     b.close()
 
 
+@pytest.mark.parametrize("host_kind", ["mapped", "torch_pinned", "pageable"])
+def test_step_host_matches_step(host_kind):
+    """ess_step_host gives the same output and state as ess_step on device
+    inputs: with mapped pinned buffers the GPU reads the inputs and writes the
+    output over the host link itself; with pageable buffers the library copies
+    through its staging."""
+    cfg = W.tiny().replace(T=2048, k=256, C=512)
+    a = Pair(cfg)
+    b = Pair(cfg)
+    keep = []
+
+    def host(arr):
+        arr = np.ascontiguousarray(arr)
+        if host_kind == "mapped":
+            hb = ess.HostBuffer(arr.shape, arr.dtype)
+            hb.array[...] = arr
+            keep.append(hb)
+            return hb
+        t = torch.from_numpy(arr.copy())
+        return t.pin_memory() if host_kind == "torch_pinned" else t
+
+    out_np = np.zeros((cfg.batch, cfg.mtp, cfg.mla_heads, 512), np.float32)
+    out_h = host(out_np)
+    for _ in range(4):
+        _, enc, w, qm = a.next_inputs(0)
+        b.next_inputs(0)
+        qd, wd, qmd = a.sess.device_inputs(enc, w, qm)
+        a.sess.step(0, qd, wd, qmd)
+        ess.ess_step_host(b.sess.pool, 0, host(enc.view(np.uint8)), host(w.astype(np.float32)),
+                          host(qm.view(np.int16)), out_h)
+        torch.cuda.synchronize()
+        assert a.sess.poll() == ess.ESS_OK and b.sess.poll() == ess.ESS_OK
+        got = out_h.array if host_kind == "mapped" else out_h.numpy()
+        assert np.array_equal(got, a.sess.out.cpu().numpy())
+        for x, y in zip(a.sess.state(0), b.sess.state(0)):
+            assert np.array_equal(x, y)
+    for hb in keep:
+        hb.close()
+    out_h = None
+    a.close()
+    b.close()
+
+
 def test_kernel_launch_count():
     """A fused step launches the indexer, the selection, the LRU finishing
     kernel, the attention and the merge; staged adds the copy."""
