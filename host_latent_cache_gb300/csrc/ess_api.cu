@@ -22,6 +22,7 @@ ess_status check_config(const ess_config* c) {
       c->mtp < 1 || c->idx_heads < 1 || c->idx_dim < 1 || c->mla_heads < 1)
     return ESS_ERR_INVALID_ARG;
   if (c->max_T % c->page != 0) return ESS_ERR_INVALID_ARG;
+  if (c->max_T % 4 != 0) return ESS_ERR_UNSUPPORTED;   // 16-byte rows of key scales
   if (!(c->sm_scale > 0.0f)) return ESS_ERR_INVALID_ARG;
   if (c->miss_mode != ESS_MISS_FUSED && c->miss_mode != ESS_MISS_STAGED) return ESS_ERR_INVALID_ARG;
   if (c->idx_dtype != ESS_FP8_E4M3 && c->idx_dtype != ESS_BF16) return ESS_ERR_INVALID_ARG;
@@ -293,13 +294,30 @@ ess_status ess_pool_destroy(ess_pool* pool) {
   return ESS_OK;
 }
 
+ess_status bind_layer(ess_pool* pool, int layer, const void* host_latent,
+                      const int32_t* page_table, const void* idx_keys, const float* idx_scale,
+                      const int32_t* T_host, bool compact);
+
 ess_status ess_pool_bind_layer(ess_pool* pool, int layer, const void* host_latent,
                                const int32_t* page_table, const void* idx_keys,
                                const float* idx_scale, const int32_t* T_host) {
+  return bind_layer(pool, layer, host_latent, page_table, idx_keys, idx_scale, T_host, false);
+}
+
+ess_status ess_pool_bind_layer_compact(ess_pool* pool, int layer, const void* host_compact,
+                                       const int32_t* page_table, const void* idx_keys,
+                                       const float* idx_scale, const int32_t* T_host) {
+  return bind_layer(pool, layer, host_compact, page_table, idx_keys, idx_scale, T_host, true);
+}
+
+ess_status bind_layer(ess_pool* pool, int layer, const void* host_latent,
+                      const int32_t* page_table, const void* idx_keys, const float* idx_scale,
+                      const int32_t* T_host, bool compact) {
   if (!pool || layer < 0 || layer >= pool->cfg.n_layers || !host_latent || !idx_keys || !T_host)
     return ESS_ERR_INVALID_ARG;
   const ess_config& c = pool->cfg;
-  if (!aligned16(idx_keys) || !aligned16(host_latent)) return ESS_ERR_INVALID_ARG;
+  if (!aligned16(idx_keys) || !aligned16(host_latent) || (idx_scale && !aligned16(idx_scale)))
+    return ESS_ERR_INVALID_ARG;
   void* dev_alias = nullptr;
   if (cudaHostGetDevicePointer(&dev_alias, const_cast<void*>(host_latent), 0) != cudaSuccess) {
     cudaGetLastError();
@@ -323,6 +341,7 @@ ess_status ess_pool_bind_layer(ess_pool* pool, int layer, const void* host_laten
   L.T0_host.assign(T_host, T_host + c.batch);
   L.n_appended = 0;
   L.host_latent = static_cast<const uint16_t*>(dev_alias);
+  L.compact = compact;
   L.page_table = page_table;
   L.idx_keys = static_cast<const uint8_t*>(idx_keys);
   L.idx_scale = idx_scale;
@@ -345,6 +364,7 @@ ess_status ess_append(ess_pool* pool, int layer, const void* latent_row, const v
   Layer& L = pool->layers[layer];
   if (!L.bound || !aligned16(latent_row) || !aligned16(key_row)) return ESS_ERR_INVALID_ARG;
   if (L.idx_scale && !key_scale) return ESS_ERR_INVALID_ARG;
+  if (L.compact) return ESS_ERR_UNSUPPORTED;   // pages would have to be encoded on the way out
   const int n = L.n_appended + 1;   // tokens appended after this call
   for (int b = 0; b < c.batch; ++b)
     if (L.T0_host[b] + n > c.max_T) return ESS_ERR_CAPACITY;

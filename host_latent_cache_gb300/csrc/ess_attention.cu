@@ -53,6 +53,7 @@ struct AttnArgs {
   int B, M, H, k, nch, C, T, page, npages;
   float c2;                   // sm_scale * log2(e)
   int staged;
+  int compact;                // host rows are compact 656-byte rows, widened on the way
   // 1: the previous kernel on the stream is the LRU finishing kernel, whose
   // own predecessor (the selection that wrote the lists read here) completed
   // before this grid could launch; the wait for the finishing kernel moves to
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int lane = tid & 31;
   bool valid = j < cnt;
   bool miss = false;
+  bool cmiss = false;          // a compact host row: widened below instead of copied
   int slot = 0;
   const uint16_t* src = nullptr;
   if (valid) {
@@ -146,6 +148,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (t < 0 || t >= Tb || slot < 0 || slot >= a.C || prow < 0 || prow >= a.T) {
       set_status(a.status, ESS_ERR_DEVICE_CHECK);
       valid = false;
+    } else if (miss && !a.staged && a.compact) {
+      cmiss = true;
+      src = reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(a.host) +
+                                              (static_cast<size_t>(b) * a.T + prow) *
+                                                  kCompactRowBytes);
     } else if (miss && !a.staged) {
       src = t >= tail_lo
                 ? a.tail + (static_cast<size_t>(b) * 2 * a.page + t % (2 * a.page)) * kRowDim
@@ -155,6 +162,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   }
   const unsigned valid_mask = __ballot_sync(0xffffffffu, valid);
+  const unsigned cmiss_mask = __ballot_sync(0xffffffffu, cmiss);
+  const unsigned copy_mask = valid_mask & ~cmiss_mask;
   const int sub = lane >> 3;   // row within a group of four
   const int ch = lane & 7;     // 16-byte chunk within the 128-byte block row
   for (int kb = 0; kb < kDimBlocks; ++kb) {
@@ -165,13 +174,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int r = warp * 32 + rl;
       const uint64_t sp = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(src), rl);
       const uint32_t off = sw128_off(r, ch);
-      if ((valid_mask >> rl) & 1u)
+      if ((copy_mask >> rl) & 1u)
         cp_async16(smem_u32(dst + off), reinterpret_cast<const uint16_t*>(sp) + kb * 64 + ch * 8);
-      else
+      else if (!((valid_mask >> rl) & 1u))
         *reinterpret_cast<uint4*>(dst + off) = make_uint4(0, 0, 0, 0);
     }
     cp_async_commit();
   }
+  // compact host rows: the warp widens its own, up to four rows' loads in flight
+  // (plain stores; each thread's fence before it publishes a block covers them)
+  for (unsigned cm = cmiss_mask; cm;) {
+    int rls[4];
+    CompactLane cl[4];
+    int nb = 0;
+    for (; nb < 4 && cm; ++nb) {
+      rls[nb] = __ffs(cm) - 1;
+      cm &= cm - 1;
+      const uint64_t sp = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(src), rls[nb]);
+      cl[nb] = compact_load(reinterpret_cast<const uint8_t*>(sp), lane);
+    }
+    for (int i = 0; i < nb; ++i) {
+      const int r = warp * 32 + rls[i];
+      uint4 lo, hi;
+      compact_widen(cl[i], lane, lo, hi);
+      // dims 16 lane .. +15: block lane / 4, 16-byte chunks 2 (lane % 4) and + 1
+      uint8_t* blk0 = rows + (lane >> 2) * kBlk;
+      *reinterpret_cast<uint4*>(blk0 + sw128_off(r, (lane & 3) * 2)) = lo;
+      *reinterpret_cast<uint4*>(blk0 + sw128_off(r, (lane & 3) * 2 + 1)) = hi;
+      if (lane >= 1 && lane < 9)   // RoPE dims 512 + 8 (lane - 1): block 8, chunk lane - 1
+        *reinterpret_cast<uint4*>(rows + 8 * kBlk + sw128_off(r, lane - 1)) = cl[i].extra;
+    }
+  }
+  __syncwarp();
   // as each 64-dim block lands: publish it; thread 0 multiplies, thread 32 refills Q
   const uint32_t idesc_qk = make_idesc(kFmtBF16, kFmtBF16, 0, 128, 128);
   bool ok = true;
@@ -422,7 +456,8 @@ __global__ void __launch_bounds__(256) stage_kernel(const int32_t* __restrict__ 
                                                     const uint16_t* __restrict__ tail,
                                                     const int32_t* __restrict__ T0,
                                                     uint16_t* __restrict__ pool, int MK, int C,
-                                                    int T, int page, int npages, int* status) {
+                                                    int T, int page, int npages, int compact,
+                                                    int* status) {
   pdl_wait_previous();
   pdl_launch_dependents();
   const int b = blockIdx.y;
@@ -436,6 +471,12 @@ __global__ void __launch_bounds__(256) stage_kernel(const int32_t* __restrict__ 
     prow = page_table[static_cast<size_t>(b) * npages + t / page] * page + t % page;
   if (t < 0 || t >= Tb[b] || v < 0 || v >= C || prow < 0 || prow >= T) {
     if (lane == 0) set_status(status, ESS_ERR_DEVICE_CHECK);
+    return;
+  }
+  if (compact) {   // a compact host row, widened to bf16 (the warp is converged here)
+    compact_row_to_bf16(reinterpret_cast<const uint8_t*>(host) +
+                            (static_cast<size_t>(b) * T + prow) * kCompactRowBytes,
+                        pool + (static_cast<size_t>(b) * C + v) * kRowDim, lane);
     return;
   }
   // appended tokens of the two newest pages come from the device ring
@@ -463,7 +504,8 @@ __global__ void __launch_bounds__(256) refill_kernel(const int32_t* __restrict__
                                                      const uint16_t* __restrict__ tail,
                                                      const int32_t* __restrict__ T0,
                                                      uint16_t* __restrict__ pool, int C, int T,
-                                                     int page, int npages, int* status) {
+                                                     int page, int npages, int compact,
+                                                     int* status) {
   const int b = blockIdx.y;
   const int s = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -476,6 +518,12 @@ __global__ void __launch_bounds__(256) refill_kernel(const int32_t* __restrict__
     prow = page_table[static_cast<size_t>(b) * npages + t / page] * page + t % page;
   if (t >= tb || prow < 0 || prow >= T) {
     if (lane == 0) set_status(status, ESS_ERR_DEVICE_CHECK);
+    return;
+  }
+  if (compact) {
+    compact_row_to_bf16(reinterpret_cast<const uint8_t*>(host) +
+                            (static_cast<size_t>(b) * T + prow) * kCompactRowBytes,
+                        pool + (static_cast<size_t>(b) * C + s) * kRowDim, lane);
     return;
   }
   const int tail_lo = max(T0[b], (tb / page - 1) * page);
@@ -542,6 +590,7 @@ cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
   a.npages = c.max_T / c.page;
   a.c2 = c.sm_scale * 1.4426950408889634f;
   a.staged = misses_staged ? 1 : 0;
+  a.compact = L.compact ? 1 : 0;
   a.early = (early && !misses_staged) ? 1 : 0;
   const size_t smem = attn_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -569,7 +618,7 @@ cudaError_t launch_stage(const ess_pool& p, int layer, const int32_t* miss_tok,
                  static_cast<const int32_t*>(L.T_dev), static_cast<const int32_t*>(L.page_table),
                  L.host_latent, static_cast<const uint16_t*>(L.tail),
                  static_cast<const int32_t*>(L.T0_dev), L.pool, MK, c.C, c.max_T, c.page,
-                 c.max_T / c.page, p.scr.status);
+                 c.max_T / c.page, L.compact ? 1 : 0, p.scr.status);
   if (e == cudaSuccess) count_launch(p);
   return e;
 }
@@ -580,7 +629,7 @@ cudaError_t launch_refill(const ess_pool& p, int layer, cudaStream_t st) {
   dim3 grid((c.C + 7) / 8, c.batch);
   refill_kernel<<<grid, 256, 0, st>>>(L.slot_token, L.T_dev, L.page_table, L.host_latent, L.tail,
                                       L.T0_dev, L.pool, c.C, c.max_T, c.page, c.max_T / c.page,
-                                      p.scr.status);
+                                      L.compact ? 1 : 0, p.scr.status);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) count_launch(p);
   return e;

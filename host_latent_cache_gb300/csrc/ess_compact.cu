@@ -8,10 +8,11 @@
 // e4m3 in four tiles of 128, one float32 scale per tile, then the 64 RoPE
 // values as bf16.
 //
-// A tile's scale is amax / 448 in float32 (1 for an all-zero tile), 448 being
-// the largest finite e4m3 value.  A value's code is its float32 quotient by
-// the scale rounded to the nearest e4m3 value, ties to the even code,
-// saturating at 448, the sign kept.  The e4m3 format: 1 sign bit, 4 exponent
+// A tile's scale is the smallest power of two at or above amax / 448 in float32
+// (1 for an all-zero tile), 448 being the largest finite e4m3 value; a power
+// of two so that every decoded value is exact in bf16.  A value's code is its
+// (exact) quotient by the scale rounded to the nearest e4m3 value, ties to the
+// even code, saturating at 448, the sign kept.  The e4m3 format: 1 sign bit, 4 exponent
 // bits with bias 7, 3 mantissa bits; exponent 0 holds the subnormals m * 2^-9;
 // the code with all exponent and mantissa bits set is NaN, so 448 (exponent
 // 15, mantissa 6) is the largest finite value.
@@ -63,7 +64,12 @@ extern "C" ess_status ess_compact_rows(const uint16_t* rows_bf16, int64_t n_rows
     for (int j = 0; j < kTiles; ++j) {
       float amax = 0.0f;
       for (int i = 0; i < kTile; ++i) amax = std::fmax(amax, std::fabs(bf16_to_float(row[j * kTile + i])));
-      const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+      float scale = 1.0f;
+      if (amax > 0.0f) {
+        int e;
+        const float fr = std::frexp(amax / 448.0f, &e);   // q = fr * 2^e, fr in [0.5, 1)
+        scale = std::ldexp(1.0f, fr == 0.5f ? e - 1 : e);
+      }
       for (int i = 0; i < kTile; ++i) {
         const float q = bf16_to_float(row[j * kTile + i]) / scale;
         dst[j * kTile + i] = e4m3_encode(q);

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "ess_internal.h"
@@ -309,6 +310,71 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
+}
+
+// ---------------------------------------------------------------- compact rows
+// A compact latent row ("ESS: Latent-Cache Offload", the ~656-byte host
+// transfers): 512 e4m3 codes in four tiles of 128, four float32 tile scales
+// (powers of two), then the 64 RoPE values as bf16.  A warp reads one row as
+// 41 16-byte chunks: lane l takes codes chunk l (dims 16l .. 16l + 15) and,
+// for l < 9, chunk 32 + l (the scales for lane 0, RoPE dims 512 + 8(l - 1)
+// .. + 7 for lanes 1..8).  Widening is exact: a code times a power of two is
+// a bf16 value.
+constexpr int kCompactRowBytes = 656;
+
+struct CompactLane {
+  uint4 codes;
+  uint4 extra;
+};
+
+__device__ __forceinline__ CompactLane compact_load(const uint8_t* row, int lane) {
+  const uint4* s = reinterpret_cast<const uint4*>(row);
+  CompactLane c;
+  c.codes = s[lane];
+  c.extra = lane < 9 ? s[32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+  return c;
+}
+
+// The lane's 16 latent dims as bf16 in two 16-byte units (all 32 lanes call it).
+__device__ __forceinline__ void compact_widen(const CompactLane& c, int lane, uint4& lo,
+                                              uint4& hi) {
+  const uint32_t s0 = __shfl_sync(0xffffffffu, c.extra.x, 0);
+  const uint32_t s1 = __shfl_sync(0xffffffffu, c.extra.y, 0);
+  const uint32_t s2 = __shfl_sync(0xffffffffu, c.extra.z, 0);
+  const uint32_t s3 = __shfl_sync(0xffffffffu, c.extra.w, 0);
+  const int t = lane >> 3;   // tile of dims 16 * lane ..
+  const float sc = __uint_as_float(t == 0 ? s0 : (t == 1 ? s1 : (t == 2 ? s2 : s3)));
+  const uint32_t w[4] = {c.codes.x, c.codes.y, c.codes.z, c.codes.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __nv_fp8x2_storage_t pair =
+          static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xffffu);
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+      __half_raw h0, h1;
+      h0.x = hr.x;
+      h1.x = hr.y;
+      const float f0 = __half2float(__half(h0)) * sc;
+      const float f1 = __half2float(__half(h1)) * sc;
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(f0, f1);
+      o[2 * i + h] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// One warp widens a compact row into a linear bf16 row of 576 values.
+__device__ __forceinline__ void compact_row_to_bf16(const uint8_t* src, uint16_t* dst, int lane) {
+  const CompactLane c = compact_load(src, lane);
+  uint4 lo, hi;
+  compact_widen(c, lane, lo, hi);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[2 * lane] = lo;
+  d[2 * lane + 1] = hi;
+  if (lane >= 1 && lane < 9) d[64 + lane - 1] = c.extra;   // RoPE: bytes 1024 + 16(lane - 1)
 }
 
 // ---------------------------------------------------------------- misc

@@ -48,6 +48,7 @@ struct IdxArgs {
 
 constexpr uint32_t kTileBytes = kIdxTile * kKeyRowBytes;  // 16 KB
 constexpr int kMaxAcc = 8;   // TMEM accumulators in flight (A * N <= 512 columns)
+constexpr int kScaleRing = 16;   // key-scale ring: one 512-byte entry per tile (>= S + A)
 
 // Walks a CTA's tiles in order over the concatenated requests: request b
 // owns tiles [lo, hi); the tile prefix is read only when the request changes.
@@ -95,7 +96,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   uint64_t* qempty = qfull + 2;
   uint64_t* epdone = qempty + 2;      // every epilogue thread has counted its tiles
   uint64_t* fldone = epdone + 2;      // the histogram is flushed and clear again
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fldone + 2);
+  uint64_t* sfull = fldone + 2;       // [kScaleRing] a tile's key scales have landed
+  uint64_t* sempty = sfull + kScaleRing;   // [kScaleRing] its epilogue group has read them
+  float* sring = reinterpret_cast<float*>(sempty + kScaleRing);   // [kScaleRing][128]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sring + kScaleRing * kIdxTile);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* consumed = abort_flag + 1;
 
@@ -123,6 +127,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       mbar_init(smem_u32(&epdone[i]), 256);
       mbar_init(smem_u32(&fldone[i]), 256);
     }
+    for (int i = 0; i < kScaleRing; ++i) {
+      mbar_init(smem_u32(&sfull[i]), 1);
+      mbar_init(smem_u32(&sempty[i]), 128);
+    }
     *abort_flag = 0;
     *consumed = 0;
     fence_mbar_init();
@@ -147,6 +155,15 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   // mode: no append kernel has run on this layer since its last indexer, so
   // the tile prefix and the key rows of the first tiles are final already and
   // the first ring's worth of key tiles is requested before the wait.
+  // the key scales of tile it (tokens t0 ..) into ring entry it % kScaleRing:
+  // 4 bytes per token, a multiple of 16 bytes since max_T is a multiple of 4
+  auto issue_scales = [&](int it, int b, int t0) {
+    const int r = it % kScaleRing;
+    const int n = a.T - t0 < kIdxTile ? a.T - t0 : kIdxTile;
+    mbar_arrive_expect_tx(smem_u32(&sfull[r]), static_cast<uint32_t>(n * 4));
+    bulk_load(smem_u32(sring + r * kIdxTile), a.scale + static_cast<size_t>(b) * a.T + t0,
+              static_cast<uint32_t>(n * 4), smem_u32(&sfull[r]));
+  };
   int n_early = 0;
   if (warp == 0 && a.early) {
     if (lane == 0) {
@@ -157,6 +174,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         mbar_arrive_expect_tx(smem_u32(&full[n_early]), kTileBytes);
         tma_load_2d(smem_u32(kst + n_early * kTileBytes), &kmap, smem_u32(&full[n_early]), 0,
                     tc.b * a.T + (g - tc.lo) * kIdxTile);
+        if (a.scale != nullptr) issue_scales(n_early, tc.b, (g - tc.lo) * kIdxTile);
       }
     }
     n_early = __shfl_sync(0xffffffffu, n_early, 0);
@@ -202,10 +220,14 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       if (lane == 0 && it >= n_early) {
         const int s = it % S;
         if (it >= S) w_ok = mbar_wait(smem_u32(&empty[s]), ((it / S) - 1) & 1, abort_flag) ? 1 : 0;
+        if (w_ok && a.scale != nullptr && it >= kScaleRing)
+          w_ok = mbar_wait(smem_u32(&sempty[it % kScaleRing]), ((it / kScaleRing) - 1) & 1,
+                           abort_flag) ? 1 : 0;
         if (w_ok) {
           mbar_arrive_expect_tx(smem_u32(&full[s]), kTileBytes);
           tma_load_2d(smem_u32(kst + s * kTileBytes), &kmap, smem_u32(&full[s]), 0,
                       b * a.T + j * kIdxTile);
+          if (a.scale != nullptr) issue_scales(it, b, j * kIdxTile);
         }
       }
       w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
@@ -222,6 +244,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       const int issued = it > n_early ? it : n_early;
       for (int i = *consumed; i < issued; ++i)
         mbar_wait(smem_u32(&full[i % S]), (i / S) & 1, nullptr);
+      // and the scale copies still in flight (the newest use of each entry)
+      if (a.scale != nullptr)
+        for (int i = issued > kScaleRing ? issued - kScaleRing : 0; i < issued; ++i)
+          mbar_wait(smem_u32(&sfull[i % kScaleRing]), (i / kScaleRing) & 1, nullptr);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
@@ -290,8 +316,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         // issue the scale load before waiting so its latency hides under the wait
         const int t = j * kIdxTile + row;
         const bool in_range = t < Tcur;
-        float sc = 1.0f;
-        if (a.scale != nullptr && in_range) sc = __ldg(a.scale + static_cast<size_t>(b) * a.T + t);
         const int acc = it % A;
         ok = mbar_wait(smem_u32(&accf[acc]), (it / A) & 1, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
@@ -363,6 +387,18 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&acce[acc]));
+        // the token's key scale, staged in shared memory with the tile
+        float sc = 1.0f;
+        if (a.scale != nullptr) {
+          const int r = it % kScaleRing;
+          if (in_range) {
+            ok = mbar_wait(smem_u32(&sfull[r]), (it / kScaleRing) & 1, abort_flag);
+            sc = sring[r * kIdxTile + row];
+          }
+          mbar_arrive(smem_u32(&sempty[r]));
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+        }
         if (in_range) {
 #pragma unroll
           for (int m = 0; m < kMaxWays; ++m) {   // unrolled: sm stays in registers
@@ -407,7 +443,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
 size_t indexer_smem_bytes(int S, int NP, int HB) {
   return 1024 + static_cast<size_t>(S) * kTileBytes + 2u * NP * 128 + 2u * NP * 4 + HB * 4u +
-         (2 * S + 2 * kMaxAcc + 8) * 8 + 16;
+         (2 * S + 2 * kMaxAcc + 8 + 2 * kScaleRing) * 8 + kScaleRing * kIdxTile * 4 + 16;
 }
 
 // Largest key ring (at most kIdxMaxStages) that fits one CTA beside the

@@ -43,6 +43,7 @@ constexpr int kStatFields = 6;        // ess_stats fields kept on the device
 struct Layer {
   bool bound = false;
   const uint16_t* host_latent = nullptr;  // device-accessible alias of the pinned host rows
+  bool compact = false;           // host rows are compact 656-byte rows (no appends)
   const int32_t* page_table = nullptr;
   const uint8_t* idx_keys = nullptr;
   const float* idx_scale = nullptr;

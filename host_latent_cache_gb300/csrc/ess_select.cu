@@ -78,6 +78,12 @@ struct SelArgs {
   int policy;                 // ESS_EVICT_*: LRU keeps the order list; the others
                               // leave the victims to victim_kernel
   unsigned long long seed;    // key of the Random victim order
+  // the layer's host rows, so that each miss's address translation starts
+  // while the selection still runs (a prefetch; nothing waits for it)
+  const uint8_t* host;        // device alias of the pinned host rows
+  const int32_t* page_table;  // [B][T/page] or null
+  const int32_t* T0;          // [B] rows t >= T0_b may still sit in the device ring
+  int page, row_bytes;
   int n_local;                // tokens per CTA (multiple of 4)
   int c_local;                // slots / order positions per CTA
   int resident;               // scores staged in shared memory
@@ -858,6 +864,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         const int t = ltok[e];
         lslot[e] = -2 - pos;   // a miss: its index in the request's miss union
         a.miss_tok[static_cast<size_t>(b) * MK + pos] = t;
+        if (a.host != nullptr && t < a.T0[b]) {
+          const int pr = a.page_table
+                             ? a.page_table[static_cast<size_t>(b) * (a.T / a.page) + t / a.page] *
+                                       a.page + t % a.page
+                             : t;
+          if (pr >= 0 && pr < a.T)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                a.host + (static_cast<size_t>(b) * a.T + pr) * a.row_bytes));
+        }
       }
     }
   }
@@ -1452,6 +1467,11 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
   a.miss_slot = miss_slot;
   a.n_miss = n_miss;
   a.vlist = p.scr.vlist;
+  a.host = reinterpret_cast<const uint8_t*>(L.host_latent);
+  a.page_table = L.page_table;
+  a.T0 = L.T0_dev;
+  a.page = c.page;
+  a.row_bytes = L.compact ? kCompactRowBytes : kRowBytes;
   a.stats = L.stats;
   a.status = p.scr.status;
   a.B = c.batch;

@@ -42,7 +42,12 @@ EXPORTS = (
     "ess_pipeline_step", "ess_pool_get_state", "ess_pool_set_state", "ess_pool_get_rows",
     "ess_pool_read_stats", "ess_pool_poll", "ess_pool_kernel_launches", "ess_prefill_plan",
     "ess_compact_rows", "ess_replay_misses", "ess_host_gather", "ess_pool_set_eviction",
+    "ess_pool_bind_layer_compact", "ess_prefill_run",
 )
+
+# void (*)(void* user, int32_t layer, void* buffer, void* stream)
+PREFILL_COMPUTE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                      ctypes.c_void_p)
 
 
 class ess_config(ctypes.Structure):
@@ -113,6 +118,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "ess_replay_misses": [I, I, P, P, P, I, I, I, ctypes.c_uint64, ctypes.c_int64, P, P],
         "ess_host_gather": [P, ctypes.c_int64, I, P, ctypes.c_int64, P, P, P],
         "ess_pool_set_eviction": [P, I, ctypes.c_uint64],
+        "ess_pool_bind_layer_compact": [P, I, P, P, P, P, P],
+        "ess_prefill_run": [I, P, I, I, P, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_size_t, P,
+                            PREFILL_COMPUTE_FN, P, P, P, P],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -209,6 +217,13 @@ def ess_pool_destroy(pool: int) -> None:
 def ess_pool_bind_layer(pool, layer, host_latent, page_table, idx_keys, idx_scale, T_host) -> None:
     check(load().ess_pool_bind_layer(pool, layer, _p(host_latent), _p(page_table), _p(idx_keys),
                                      _p(idx_scale), _p(T_host)), "ess_pool_bind_layer")
+
+
+def ess_pool_bind_layer_compact(pool, layer, host_compact, page_table, idx_keys, idx_scale,
+                                T_host) -> None:
+    check(load().ess_pool_bind_layer_compact(pool, layer, _p(host_compact), _p(page_table),
+                                             _p(idx_keys), _p(idx_scale), _p(T_host)),
+          "ess_pool_bind_layer_compact")
 
 
 def ess_pool_reset(pool, layer, stream=None) -> None:
@@ -375,3 +390,22 @@ def ess_pool_set_eviction(pool, policy: int, seed: int = 0) -> None:
     """Victim order of the decode kernels (ESS_EVICT_*)."""
     check(load().ess_pool_set_eviction(pool, int(policy), seed & ((1 << 64) - 1)),
           "ess_pool_set_eviction")
+
+
+def ess_prefill_run(onload_layer_map, host_kv, layer_bytes: int, buffers, compute,
+                    compute_stream, h2d_stream, d2h_stream, rotating: int = 3,
+                    shared_copy: bool = False, wb_offset: int = 0, wb_bytes=None) -> None:
+    """One prefill pass.  host_kv: per layer a pinned host buffer (HostBuffer or
+    tensor; entry 0 may be None); buffers: 1 + rotating device tensors;
+    compute(layer, buffer_ptr, stream_ptr) enqueues the layer's work."""
+    import numpy as np
+    m = np.ascontiguousarray(onload_layer_map, dtype=np.int32)
+    L = int(m.shape[0])
+    hk = (ctypes.c_void_p * L)(*[None if h is None else _p(h) for h in host_kv])
+    bf = (ctypes.c_void_p * len(buffers))(*[_p(b) for b in buffers])
+    cb = PREFILL_COMPUTE_FN(lambda user, layer, buf, st: compute(int(layer), buf, st))
+    wb = layer_bytes - wb_offset if wb_bytes is None else wb_bytes
+    check(load().ess_prefill_run(L, m.ctypes.data, int(rotating), int(bool(shared_copy)), hk,
+                                 int(layer_bytes), int(wb_offset), int(wb), bf, cb, None,
+                                 _stream(compute_stream), _stream(h2d_stream),
+                                 _stream(d2h_stream)), "ess_prefill_run")

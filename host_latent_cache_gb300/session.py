@@ -49,11 +49,12 @@ class Session:
             if host_buffers is not None:
                 host = host_buffers[l]
             else:
-                host = ess.HostBuffer(ld.host_latent.shape, np.uint16)
+                host = ess.HostBuffer(ld.host_latent.shape, ld.host_latent.dtype)
                 host.array[...] = ld.host_latent
                 self._own_host.append(host)
             T = torch.from_numpy(ld.T.astype(np.int32))
-            ess.ess_pool_bind_layer(self.pool, l, host, pages, keys, scale, T)
+            bind = ess.ess_pool_bind_layer_compact if cfg.compact else ess.ess_pool_bind_layer
+            bind(self.pool, l, host, pages, keys, scale, T)
             self.keys.append(keys)
             self.scale.append(scale)
             self.pages.append(pages)

@@ -155,6 +155,7 @@ class WorkloadConfig:
     seed: int = 1000
     T_per_req: Optional[List[int]] = None   # ragged contexts (defaults to T for all)
     grow: int = 0               # tokens appended to every request, one per step
+    compact: bool = False       # host latent as compact 656-byte rows (e4m3 + scales + bf16 RoPE)
     sm_scale: float = float(np.float32(1.0 / np.sqrt(576.0)))
 
     def t_of(self, b: int) -> int:
@@ -231,6 +232,7 @@ class LayerData:
     T: np.ndarray
     app_keys: Optional[np.ndarray] = None
     app_scale: Optional[np.ndarray] = None
+    latent_c: Optional[np.ndarray] = None   # compact rows uint8 [B][T_max][656], logical order
 
 
 def t_max_of(cfg: WorkloadConfig) -> int:
@@ -292,6 +294,11 @@ def gen_layer(cfg: WorkloadConfig, layer: int = 0, want_latent: bool = True) -> 
             phys = pages[b][t // cfg.page] * cfg.page + (t % cfg.page)
             host[b][phys] = latent[b]
     Ts = np.array([cfg.t_of(b) for b in range(B)], dtype=np.int32)
+    if cfg.compact:
+        if cfg.grow:
+            raise ValueError("compact host rows take no appends")
+        latent_c, host = gen_compact_latent(cfg, layer, pages) if want_latent else (None, None)
+        return LayerData(keys, scale, w, None, host, pages, Ts, None, None, latent_c)
     app_keys = app_scale = None
     if cfg.grow > 0:
         app_keys = np.zeros((B, cfg.grow, rb), dtype=np.uint8)
@@ -309,6 +316,8 @@ def gen_layer(cfg: WorkloadConfig, layer: int = 0, want_latent: bool = True) -> 
 
 
 _TID_STATE = 8
+_TID_COMPACT = 9
+COMPACT_ROW_BYTES = 656
 
 
 @dataclass
@@ -344,6 +353,30 @@ def full_pool_state(cfg: WorkloadConfig, ld: LayerData, layer: int = 0,
         cs[b, toks] = slots
         lu[b, slots] = r.integers(0, age, size=n).astype(np.int32)
     return PoolState(cs, st, lu, sp)
+
+
+def gen_compact_latent(cfg: WorkloadConfig, layer: int, pages: np.ndarray):
+    """Compact latent rows drawn directly in their stored form (logical order,
+    and the page-permuted host copy): per token, 512 e4m3 codes (a random
+    sign and a magnitude code uniform over the finite codes 0x00..0x7E, i.e.
+    values spread log-uniformly from 2^-9 to 448), four tile scales 2^-9,
+    2^-8 or 2^-7, and 64 RoPE values bf16 N(0, 0.5)."""
+    B, Tm, page = cfg.batch, t_max_of(cfg), cfg.page
+    lat = np.zeros((B, Tm, COMPACT_ROW_BYTES), dtype=np.uint8)
+    host = np.zeros_like(lat)
+    for b in range(B):
+        r = _rng(cfg.seed, _TID_COMPACT, layer, b)
+        mag = r.integers(0, 0x7F, size=(Tm, 512), dtype=np.uint8)
+        sign = (r.integers(0, 2, size=(Tm, 512), dtype=np.uint8) << np.uint8(7)).astype(np.uint8)
+        lat[b, :, :512] = mag | sign
+        sc = np.ldexp(np.float32(1.0), r.integers(-9, -6, size=(Tm, 4))).astype("<f4")
+        lat[b, :, 512:528] = sc.view(np.uint8).reshape(Tm, 16)
+        rope = r.standard_normal((Tm, ROPE_DIM), dtype=np.float32) * np.float32(0.5)
+        lat[b, :, 528:] = float_to_bf16_bits(rope).reshape(Tm, ROPE_DIM).astype("<u2").view(
+            np.uint8).reshape(Tm, 2 * ROPE_DIM)
+        t = np.arange(Tm)
+        host[b][pages[b][t // page] * page + t % page] = lat[b]
+    return lat, host
 
 
 def appended_token(cfg: WorkloadConfig, ld: LayerData, i: int):

@@ -81,6 +81,7 @@ typedef struct {
   int32_t n_layers;    /* layers held by this pool                            */
   int32_t batch;       /* B requests                                          */
   int32_t max_T;       /* T: context capacity per request, a multiple of page */
+                       /* and of 4                                            */
   int32_t C;           /* hot-pool slots per request and layer ([FO] C_b)     */
   int32_t page;        /* host page size in tokens (block-table granularity)  */
   int32_t k;           /* top-k per way ([FO]: k = 2048)                      */
@@ -162,6 +163,22 @@ ess_status ess_pool_bind_layer(ess_pool* pool, int layer, const void* host_laten
                                const int32_t* page_table, const void* idx_keys,
                                const float* idx_scale, const int32_t* T_host);
 
+/* ess_pool_bind_layer with the host master copy held as compact 656-byte
+ * rows (the format of ess_compact_rows): 512 e4m3 latent values in four tiles
+ * with power-of-two float32 scales, then the 64 RoPE values as bf16
+ * ("ESS: Latent-Cache Offload", the ~656-byte FlashTrans + UVA transfers).
+ *   host_compact  pinned host [B][T][656] bytes, physical rows through the
+ *                 page table as for ess_pool_bind_layer
+ * A miss moves 656 bytes over the host link instead of 1152: the gathers
+ * (fused attention, staging, and the reload of ess_pool_set_state) widen the
+ * row to bf16 on the way, exactly (a code times a power of two is a bf16
+ * value), and the hot pool keeps bf16 rows, so hits and the attention
+ * arithmetic are unchanged.  ess_append is refused (ESS_ERR_UNSUPPORTED) on
+ * such a layer.  Errors as ess_pool_bind_layer. */
+ess_status ess_pool_bind_layer_compact(ess_pool* pool, int layer, const void* host_compact,
+                                       const int32_t* page_table, const void* idx_keys,
+                                       const float* idx_scale, const int32_t* T_host);
+
 /* Empty the hot pool of a layer again (asynchronous on stream). */
 ess_status ess_pool_reset(ess_pool* pool, int layer, ess_stream_t stream);
 
@@ -183,7 +200,8 @@ ess_status ess_pool_reset(ess_pool* pool, int layer, ess_stream_t stream);
  * the step that should see the token.  Asynchronous on stream (one kernel).
  * Errors: ESS_ERR_CAPACITY, launching nothing, when a request is already at
  * max_T; ESS_ERR_INVALID_ARG for an unbound layer, a null or misaligned
- * row, or a missing key_scale. */
+ * row, or a missing key_scale; ESS_ERR_UNSUPPORTED on a layer bound with
+ * compact rows. */
 ess_status ess_append(ess_pool* pool, int layer, const void* latent_row, const void* key_row,
                       const float* key_scale, ess_stream_t stream);
 
@@ -414,9 +432,10 @@ ess_status ess_replay_misses(int32_t n_steps, int32_t n_ways, const int64_t* off
  * 83.2% indexer/latent byte split).  Layout (a reading; the page gives only
  * the size): bytes 0..511 the 512 latent values as e4m3 in four tiles of 128,
  * bytes 512..527 one little-endian float32 scale per tile, bytes 528..655 the
- * 64 RoPE values as bf16.  A tile's scale is fl32(amax / 448) (1 for an
- * all-zero tile); a value's code is e4m3(fl32(x / scale)), nearest with ties
- * to the even code, saturating at +-448, sign kept.  Host code only.
+ * 64 RoPE values as bf16.  A tile's scale is the smallest power of two at or
+ * above fl32(amax / 448) (1 for an all-zero tile), so every decoded value is
+ * exact in bf16; a value's code is e4m3(x / scale), nearest with ties to the
+ * even code, saturating at +-448, sign kept.
  *   rows_bf16  host bf16 [n_rows][576]
  *   out        host uint8 [n_rows][656]
  * Errors: ESS_ERR_INVALID_ARG for n_rows < 0 or a null buffer. */
@@ -426,7 +445,7 @@ ess_status ess_compact_rows(const uint16_t* rows_bf16, int64_t n_rows, uint8_t* 
  * buffers ([FO] "prefill side": B0 pinned to layer 0, B1..B3 rotating through
  * a binding table, a buffer reused only after its layer's compute and
  * write-back, layer onload_layer_map[i] prefetched at layer i's scheduling
- * point).  Host code only; it plans, it moves nothing.
+ * point).  Host code; it plans, ess_prefill_run moves the data.
  *   n_layers          L >= 1
  *   onload_layer_map  host int32 [L]: the layer (1..L-1) prefetched at layer
  *                     i's scheduling point, or -1; a layer no entry names is
@@ -445,6 +464,39 @@ ess_status ess_compact_rows(const uint16_t* rows_bf16, int64_t n_rows, uint8_t* 
 ess_status ess_prefill_plan(int32_t n_layers, const int32_t* onload_layer_map, int32_t rotating,
                             int32_t shared_copy, int32_t* buffer, int32_t* load_at,
                             int32_t* reuse_after);
+
+/* Per-layer compute of a prefill pass, called by ess_prefill_run on the
+ * calling thread: enqueue the layer's work on `stream` (asynchronously); it
+ * may read and update `buffer`, the device buffer that holds the layer's KV. */
+typedef void (*ess_prefill_compute_fn)(void* user, int32_t layer, void* buffer,
+                                       ess_stream_t stream);
+
+/* One prefill pass over n_layers layers with whole-layer device buffers, run
+ * by the schedule of ess_prefill_plan ([FO] "prefill side: four whole-layer
+ * buffers hide the transfers", its five-step lifecycle and Figure 3):
+ *   buffers      device [1 + rotating] buffers of layer_bytes each; buffers[0]
+ *                (B0) holds layer 0 throughout and is neither loaded nor
+ *                written back here; B1.. rotate over layers 1..L-1
+ *   host_kv      pinned host [L] pointers, layer l's KV (layer_bytes each;
+ *                host_kv[0] unused)
+ *   compute      the caller's per-layer work, called in layer order
+ *   wb_offset, wb_bytes  the byte range of a layer written back after its
+ *                compute (e.g. the rows this pass produced)
+ * Layer j is loaded (H2D on h2d_stream) up front, or at the scheduling point
+ * of the layer that prefetches it, once the previous layer of its buffer has
+ * been computed and written back; compute(i) waits for layer i's load; the
+ * write-back (D2H on d2h_stream, or on h2d_stream when shared_copy) follows
+ * compute(i) and releases the buffer.  Events carry every dependency, so the
+ * copies overlap the computes of other layers.  Asynchronous: when
+ * compute_stream has passed the call, every write-back is done.
+ * Errors: ESS_ERR_INVALID_ARG for a bad argument or a schedule that
+ * ess_prefill_plan refuses; ESS_ERR_CUDA when a CUDA call fails. */
+ess_status ess_prefill_run(int32_t n_layers, const int32_t* onload_layer_map, int32_t rotating,
+                           int32_t shared_copy, void* const* host_kv, size_t layer_bytes,
+                           size_t wb_offset, size_t wb_bytes, void* const* buffers,
+                           ess_prefill_compute_fn compute, void* user,
+                           ess_stream_t compute_stream, ess_stream_t h2d_stream,
+                           ess_stream_t d2h_stream);
 
 /* Synchronise stream, return the first device-side error since the last
  * poll (ESS_OK if none) and clear it. */

@@ -15,13 +15,16 @@ do not lay the 656 bytes out; the reading taken here (656 = 512 + 16 + 128):
   bytes 512..527  one float32 scale per tile (little-endian);
   bytes 528..655  the 64 RoPE values, bf16 as they were.
 
-Encoding a tile: scale = fl32(amax / 448) (1 when the tile is all zero),
-where amax is the largest magnitude in the tile and 448 the largest finite
-e4m3 value.  Each value becomes e4m3(fl32(x / scale)), rounded to nearest
-with ties to the even code and saturated at +-448; the sign of a value that
-rounds to zero is kept.  The quotient is a float32 division, as a GPU
-encoder would do it, so the code that fp32 arithmetic decides is the one
-stored.  The row's value is code * scale, exact in float64.
+Encoding a tile: its scale is the smallest power of two at or above
+fl32(amax / 448) (1 when the tile is all zero), where amax is the largest
+magnitude in the tile and 448 the largest finite e4m3 value; a power of two,
+like the shared block exponents of the OCP microscaling (MX) formats, so that
+every decoded value code * scale is exact in bf16 and a GPU can widen a row
+into the bf16 operands of its attention without rounding.  Each value becomes
+e4m3(x / scale) (exact division), rounded to nearest with ties to the even
+code; the largest magnitude lands in (224, 448], and anything at or above 448
+saturates there; the sign of a value that rounds to zero is kept.  The row's
+value is code * scale, exact in float64 and in bf16.
 """
 from __future__ import annotations
 
@@ -68,6 +71,15 @@ def e4m3_encode(v: float) -> int:
     return sign | int(_POS_CODES[hi])
 
 
+def tile_scale(amax: np.float32) -> np.float32:
+    """The smallest power of two >= fl32(amax / 448); 1 for amax = 0."""
+    if not amax > 0:
+        return np.float32(1.0)
+    q = np.float32(np.float32(amax) / np.float32(E4M3_MAX))
+    m, e = np.frexp(q)                                  # q = m * 2^e, m in [0.5, 1)
+    return np.float32(np.ldexp(1.0, int(e) - 1) if m == 0.5 else np.ldexp(1.0, int(e)))
+
+
 def encode_row(bits: np.ndarray) -> np.ndarray:
     """bf16 bits [576] of one latent row -> uint8 [656]."""
     bits = np.asarray(bits, dtype=np.uint16)
@@ -76,10 +88,9 @@ def encode_row(bits: np.ndarray) -> np.ndarray:
     scales = np.zeros(LATENT // TILE, dtype=np.float32)
     for j in range(LATENT // TILE):
         tile = x[j * TILE:(j + 1) * TILE]
-        amax = np.float32(np.max(np.abs(tile)))
-        scale = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
+        scale = tile_scale(np.float32(np.max(np.abs(tile))))
         scales[j] = scale
-        q = (tile / scale).astype(np.float32)           # one float32 division per value
+        q = (tile / scale).astype(np.float32)           # exact: the scale is a power of two
         out[j * TILE:(j + 1) * TILE] = [e4m3_encode(float(v)) for v in q]
     out[LATENT:LATENT + 16] = scales.astype("<f4").view(np.uint8)
     out[LATENT + 16:] = bits[LATENT:].astype("<u2").view(np.uint8)
@@ -95,3 +106,17 @@ def decode_row(row: np.ndarray) -> np.ndarray:
     rope_bits = row[LATENT + 16:].view("<u2").astype(np.uint32) << np.uint32(16)
     rope = rope_bits.view(np.float32).astype(np.float64)
     return np.concatenate([lat, rope])
+
+
+_CODE_VALUES = np.array([e4m3_value(c) for c in range(256)])   # NaN for 0x7F, 0xFF
+
+
+def decode_rows(rows: np.ndarray) -> np.ndarray:
+    """uint8 [n][656] -> float64 [n][576]: decode_row for many rows at once
+    (a table lookup of the codes times each tile's scale)."""
+    rows = np.ascontiguousarray(rows, dtype=np.uint8).reshape(-1, ROW_BYTES)
+    scales = rows[:, LATENT:LATENT + 16].copy().view("<f4").astype(np.float64)   # [n][4]
+    lat = _CODE_VALUES[rows[:, :LATENT]] * np.repeat(scales, TILE, axis=1)
+    rope_bits = rows[:, LATENT + 16:].copy().view("<u2").astype(np.uint32) << np.uint32(16)
+    rope = rope_bits.view(np.float32).astype(np.float64)
+    return np.concatenate([lat, rope], axis=1)

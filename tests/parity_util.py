@@ -7,6 +7,7 @@ import torch
 from host_latent_cache_gb300 import ess
 from host_latent_cache_gb300 import workloads as W
 from host_latent_cache_gb300.session import Session
+from oracle import compact_row as X
 from oracle import ess_oracle as O
 
 # attention tolerance: max-abs error and relative L2 error against the float64 oracle
@@ -58,7 +59,10 @@ class Pair:
         ld = self.lds[layer]
         keys = self.keys32[layer]
         keyf = lambda b: keys[b, : int(ld.T[b])]
-        latf = lambda b, order: W.bf16_bits_to_float(ld.latent[b, order]).astype(np.float64)
+        if self.cfg.compact:
+            latf = lambda b, order: X.decode_rows(ld.latent_c[b, order])
+        else:
+            latf = lambda b, order: W.bf16_bits_to_float(ld.latent[b, order]).astype(np.float64)
         return keyf, latf
 
     def next_inputs(self, layer):
@@ -143,7 +147,13 @@ class Pair:
         for b in range(self.cfg.batch):
             o = self.orc[layer].state[b]
             occ = np.nonzero(o.slot_token >= 0)[0]
-            assert np.array_equal(rows[b, occ], ld.latent[b, o.slot_token[occ]]), f"pool rows b={b}"
+            if self.cfg.compact:
+                # the widened rows: decoded values, exact in bf16
+                dec = X.decode_rows(ld.latent_c[b, o.slot_token[occ]]).astype(np.float32)
+                want = W.float_to_bf16_bits(dec).reshape(len(occ), -1)
+            else:
+                want = ld.latent[b, o.slot_token[occ]]
+            assert np.array_equal(rows[b, occ], want), f"pool rows b={b}"
 
     def close(self):
         self.sess.close()

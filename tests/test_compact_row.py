@@ -2,11 +2,12 @@
 plausible mistakes they catch.
 
 The row is a reading of the "ESS: Latent-Cache Offload" page: 512 e4m3
-latent values in four scaled tiles, four float32 scales and the 64 bf16 RoPE
-values.  The pins: the page's byte split, the e4m3 definition (every byte's
-value, rounding to nearest with ties to the even code, saturation), exact
-round trips of values already on the scaled grid, the rounding error bound,
-and the layout of the bytes.
+latent values in four tiles with power-of-two scales, four float32 scales
+and the 64 bf16 RoPE values.  The pins: the page's byte split, the e4m3
+definition (every byte's value, rounding to nearest with ties to the even
+code, saturation), exact round trips of values already on the scaled grid,
+the scale rule and the rounding error bound, decoded values exact in bf16,
+the batched decoder against the per-row one, and the layout of the bytes.
 """
 import inspect
 import os
@@ -100,7 +101,12 @@ def test_rounding_error_bound_and_layout():
         for j in range(4):
             t = slice(128 * j, 128 * (j + 1))
             amax = np.max(np.abs(xv[t]))
-            assert scales[j] == np.float32(np.float32(amax) / np.float32(448.0))
+            # the smallest power of two at or above amax / 448 (float32)
+            m, e = np.frexp(scales[j])
+            assert m == 0.5
+            q = np.float32(np.float32(amax) / np.float32(448.0))
+            assert scales[j] >= q and scales[j] / 2 < q
+            assert 224.0 < amax / scales[j] <= 448.0
             err = np.abs(dec[t] - xv[t])
             # half a step: 2^-4 of the value in the normal range, 2^-10 of the
             # scale in the subnormal range (plus the float32 division's rounding)
@@ -108,6 +114,30 @@ def test_rounding_error_bound_and_layout():
             assert np.all(err <= bound)
         assert np.array_equal(enc[528:].view("<u2"), bits[512:])          # RoPE untouched
         assert np.array_equal(dec[512:], xv[512:])
+
+
+def test_decoded_values_are_exact_in_bf16():
+    # the point of power-of-two scales: a GPU widens rows to bf16 exactly
+    rng = np.random.default_rng(5)
+    for _ in range(10):
+        x = (rng.standard_normal(576) * rng.choice([0.01, 0.5, 40.0])).astype(np.float32)
+        dec = X.decode_row(X.encode_row(_bits(x)))
+        f32 = dec.astype(np.float32)
+        assert np.array_equal(f32.astype(np.float64), dec)
+        assert np.array_equal(W.bf16_bits_to_float(_bits(f32)), f32)
+
+
+def test_decode_rows_equals_decode_row():
+    rng = np.random.default_rng(6)
+    rows = rng.integers(0, 256, size=(7, 656), dtype=np.uint8)
+    rows[:, :512] &= 0xFE                               # no NaN codes (0x7F / 0xFF)
+    rows[:, 512:528] = np.repeat(np.array([[2.0 ** -8, 0.5, 1.0, 2.0 ** 3]], "<f4").view(np.uint8),
+                                 7, axis=0)
+    rope = _bits(rng.standard_normal((7, 64)).astype(np.float32))
+    rows[:, 528:] = rope.astype("<u2").view(np.uint8).reshape(7, 128)
+    got = X.decode_rows(rows)
+    for i in range(7):
+        assert np.array_equal(got[i], X.decode_row(rows[i]))
 
 
 def test_zero_tile_has_unit_scale():
@@ -161,6 +191,18 @@ def _row_wrong_max(bits):
     return out
 
 
+def _row_scale_not_a_power_of_two(bits):
+    x = W.bf16_bits_to_float(np.asarray(bits, np.uint16))
+    out = ORIG_ROW(bits)
+    for j in range(4):
+        t = x[128 * j:128 * (j + 1)]
+        amax = np.float32(np.max(np.abs(t)))
+        s = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+        out[128 * j:128 * (j + 1)] = [ORIG_ENCODE(float(v)) for v in (t / s).astype(np.float32)]
+        out[512 + 4 * j:516 + 4 * j] = np.array([s], "<f4").view(np.uint8)
+    return out
+
+
 def _row_rope_quantized(bits):
     out = ORIG_ROW(bits)
     out[528:] = 0
@@ -169,7 +211,7 @@ def _row_rope_quantized(bits):
 
 MUTANTS = [("e4m3_encode", _encode_truncates), ("e4m3_encode", _encode_ties_away),
            ("encode_row", _row_one_scale), ("encode_row", _row_wrong_max),
-           ("encode_row", _row_rope_quantized)]
+           ("encode_row", _row_rope_quantized), ("encode_row", _row_scale_not_a_power_of_two)]
 PINS = [f for name, f in sorted(vars(sys.modules[__name__]).items())
         if name.startswith("test_") and inspect.isfunction(f) and name != "test_pins_catch_mutant"]
 

@@ -34,7 +34,7 @@ _layer_cache = {}
 
 def _layer(cfg):
     """Layer data, generated once per shape (the hot-pool size is not part of it)."""
-    key = (cfg.name.split("_C")[0], cfg.seed, cfg.batch, cfg.T)
+    key = (cfg.name.split("_C")[0], cfg.seed, cfg.batch, cfg.T, cfg.compact)
     if key not in _layer_cache:
         _layer_cache.clear()
         _layer_cache[key] = W.gen_layer(cfg)
@@ -66,6 +66,11 @@ def test_long_128k_first_steps_then_full_pool():
 @pytest.mark.parametrize("C", [8192, 16384])
 def test_ctx_1m_then_full_pool(C):
     _empty_then_full(W.ctx_1m(C), 2)
+
+
+def test_long_128k_compact_rows_then_full_pool():
+    """The 128K layer with its host copy in compact 656-byte rows."""
+    _empty_then_full(W.long_128k().replace(compact=True), 2, check_scores_first=False)
 
 
 def test_v32_full_batch_then_full_pool():
