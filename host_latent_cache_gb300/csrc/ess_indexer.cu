@@ -42,7 +42,8 @@ struct IdxArgs {
   uint32_t* ghist;           // [B][M][kHistBins] or null
   int* status;
   int B, M, HI, NP, T, total_tiles, A;
-  int S;                     // key-ring stages
+  int S;                     // key-ring stages (chunks)
+  int U;                     // tiles per chunk, the unit of the barrier rounds
   int early;                 // 1: no append since the last indexer launch on this layer
 };
 
@@ -72,6 +73,32 @@ struct TileCursor {
   }
 };
 
+// Walks a CTA's tiles in chunks of up to U consecutive tiles of one request
+// (the unit of every barrier round below), identically in every role.
+struct ChunkWalker {
+  TileCursor tc;
+  int g, g1, U;
+  __device__ __forceinline__ void start(const int32_t* off, int B, int g0_, int g1_, int U_) {
+    tc.start(off, B, g0_);
+    g = g0_;
+    g1 = g1_;
+    U = U_;
+  }
+  // request b, its first tile j0 in the chunk, n tiles; the chunk ends the
+  // request's run of tiles in this CTA when last is set
+  __device__ __forceinline__ bool next(int& b, int& j0, int& n, bool& last) {
+    if (g >= g1) return false;
+    tc.advance(g);
+    b = tc.b;
+    j0 = g - tc.lo;
+    const int end = tc.hi < g1 ? tc.hi : g1;
+    n = end - g < U ? end - g : U;
+    g += n;
+    last = g >= end;
+    return true;
+  }
+};
+
 template <bool FP8>
 __global__ void __launch_bounds__(kIdxThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
@@ -82,24 +109,26 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   const int NP = a.NP;
   const int A = a.A;
   const int S = a.S;
-  uint8_t* kst = smem;                                   // S x 16 KB key tiles
-  uint8_t* qbuf = kst + S * kTileBytes;                  // 2 x NP x 128 B queries
+  const int U = a.U;
+  const uint32_t stage_bytes = static_cast<uint32_t>(U) * kTileBytes;
+  uint8_t* kst = smem;                                   // S x U x 16 KB key tiles
+  uint8_t* qbuf = kst + S * stage_bytes;                 // 2 x NP x 128 B queries
   float* wbuf = reinterpret_cast<float*>(qbuf + 2 * NP * 128);  // 2 x NP weights
   uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + 2 * NP);   // M x kHistBins
   const int HB = a.ghist ? a.M * kHistBins : 0;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(hist + HB);
+  float* sring = reinterpret_cast<float*>(hist + HB);   // [kScaleRing][U x 128] key scales
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sring + kScaleRing * U * kIdxTile);
   uint64_t* full = bars;
   uint64_t* empty = full + S;
   uint64_t* accf = empty + S;
   uint64_t* acce = accf + kMaxAcc;
   uint64_t* qfull = acce + kMaxAcc;
   uint64_t* qempty = qfull + 2;
-  uint64_t* epdone = qempty + 2;      // every epilogue thread has counted its tiles
+  uint64_t* epdone = qempty + 2;      // every epilogue thread has counted its tokens
   uint64_t* fldone = epdone + 2;      // the histogram is flushed and clear again
-  uint64_t* sfull = fldone + 2;       // [kScaleRing] a tile's key scales have landed
+  uint64_t* sfull = fldone + 2;       // [kScaleRing] a chunk's key scales have landed
   uint64_t* sempty = sfull + kScaleRing;   // [kScaleRing] its epilogue group has read them
-  float* sring = reinterpret_cast<float*>(sempty + kScaleRing);   // [kScaleRing][128]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sring + kScaleRing * kIdxTile);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + kScaleRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* consumed = abort_flag + 1;
 
@@ -138,7 +167,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   for (int i = tid; i < HB; i += kIdxThreads) hist[i] = 0;
   for (int i = tid; i < 2 * NP; i += kIdxThreads) wbuf[i] = 0.0f;
   uint32_t ncols = 32;
-  while (ncols < static_cast<uint32_t>(A * NP)) ncols <<= 1;
+  while (ncols < static_cast<uint32_t>(A * U * NP)) ncols <<= 1;
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), ncols);
     tmem_relinquish();
@@ -151,31 +180,35 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // everything above touched only this CTA's shared memory and TMEM.  Early
-  // mode: no append kernel has run on this layer since its last indexer, so
-  // the tile prefix and the key rows of the first tiles are final already and
-  // the first ring's worth of key tiles is requested before the wait.
-  // the key scales of tile it (tokens t0 ..) into ring entry it % kScaleRing:
-  // 4 bytes per token, a multiple of 16 bytes since max_T is a multiple of 4
-  auto issue_scales = [&](int it, int b, int t0) {
-    const int r = it % kScaleRing;
-    const int n = a.T - t0 < kIdxTile ? a.T - t0 : kIdxTile;
-    mbar_arrive_expect_tx(smem_u32(&sfull[r]), static_cast<uint32_t>(n * 4));
-    bulk_load(smem_u32(sring + r * kIdxTile), a.scale + static_cast<size_t>(b) * a.T + t0,
-              static_cast<uint32_t>(n * 4), smem_u32(&sfull[r]));
+  // the keys (and key scales) of chunk it: n tiles from tile j0 of request b
+  // into stage it % S; the scales, 4 bytes per token (a multiple of 16 bytes,
+  // since max_T is a multiple of 4), into ring entry it % kScaleRing
+  auto issue_chunk = [&](int it, int b, int j0, int n) {
+    const int s = it % S;
+    mbar_arrive_expect_tx(smem_u32(&full[s]), static_cast<uint32_t>(n) * kTileBytes);
+    for (int u = 0; u < n; ++u)
+      tma_load_2d(smem_u32(kst + s * stage_bytes + u * kTileBytes), &kmap, smem_u32(&full[s]), 0,
+                  b * a.T + (j0 + u) * kIdxTile);
+    if (a.scale != nullptr) {
+      const int r = it % kScaleRing;
+      const int t0 = j0 * kIdxTile;
+      const int nt = a.T - t0 < n * kIdxTile ? a.T - t0 : n * kIdxTile;
+      mbar_arrive_expect_tx(smem_u32(&sfull[r]), static_cast<uint32_t>(nt * 4));
+      bulk_load(smem_u32(sring + r * U * kIdxTile), a.scale + static_cast<size_t>(b) * a.T + t0,
+                static_cast<uint32_t>(nt * 4), smem_u32(&sfull[r]));
+    }
   };
+  // Early mode: no append kernel has run on this layer since its last indexer,
+  // so the tile prefix and the key rows (and scales) of the first chunks are
+  // final already; the first ring's worth is requested before the wait.
   int n_early = 0;
   if (warp == 0 && a.early) {
     if (lane == 0) {
-      TileCursor tc;
-      tc.start(a.tile_off, a.B, g0);
-      for (int g = g0; g < g1 && n_early < S; ++g, ++n_early) {
-        tc.advance(g);
-        mbar_arrive_expect_tx(smem_u32(&full[n_early]), kTileBytes);
-        tma_load_2d(smem_u32(kst + n_early * kTileBytes), &kmap, smem_u32(&full[n_early]), 0,
-                    tc.b * a.T + (g - tc.lo) * kIdxTile);
-        if (a.scale != nullptr) issue_scales(n_early, tc.b, (g - tc.lo) * kIdxTile);
-      }
+      ChunkWalker cw;
+      cw.start(a.tile_off, a.B, g0, g1, U);
+      int b, j0, n;
+      bool last;
+      while (n_early < S && cw.next(b, j0, n, last)) issue_chunk(n_early++, b, j0, n);
     }
     n_early = __shfl_sync(0xffffffffu, n_early, 0);
   }
@@ -184,14 +217,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------ producer
-    TileCursor tc;
-    tc.start(a.tile_off, a.B, g0);
+    ChunkWalker cw;
+    cw.start(a.tile_off, a.B, g0, g1, U);
     int cur_b = -1, seg = -1, it = 0;
+    int b, j0, n;
+    bool last;
     bool ok = true;
-    for (int g = g0; g < g1 && ok; ++g, ++it) {
-      tc.advance(g);
-      const int b = tc.b;
-      const int j = g - tc.lo;
+    for (; ok && cw.next(b, j0, n, last); ++it) {
       if (b != cur_b) {
         ++seg;
         const int qb = seg & 1;
@@ -223,12 +255,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (w_ok && a.scale != nullptr && it >= kScaleRing)
           w_ok = mbar_wait(smem_u32(&sempty[it % kScaleRing]), ((it / kScaleRing) - 1) & 1,
                            abort_flag) ? 1 : 0;
-        if (w_ok) {
-          mbar_arrive_expect_tx(smem_u32(&full[s]), kTileBytes);
-          tma_load_2d(smem_u32(kst + s * kTileBytes), &kmap, smem_u32(&full[s]), 0,
-                      b * a.T + j * kIdxTile);
-          if (a.scale != nullptr) issue_scales(it, b, j * kIdxTile);
-        }
+        if (w_ok) issue_chunk(it, b, j0, n);
       }
       w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
       if (!w_ok) ok = false;
@@ -239,12 +266,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         *abort_flag = 1;
       }
     }
-    // drain: wait (bounded) for every issued tile load to land
+    // drain: wait (bounded) for every issued copy to land
     if (lane == 0 && *abort_flag) {
       const int issued = it > n_early ? it : n_early;
       for (int i = *consumed; i < issued; ++i)
         mbar_wait(smem_u32(&full[i % S]), (i / S) & 1, nullptr);
-      // and the scale copies still in flight (the newest use of each entry)
       if (a.scale != nullptr)
         for (int i = issued > kScaleRing ? issued - kScaleRing : 0; i < issued; ++i)
           mbar_wait(smem_u32(&sfull[i % kScaleRing]), (i / kScaleRing) & 1, nullptr);
@@ -254,12 +280,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = FP8 ? make_idesc(kFmtE4M3, kFmtE4M3, 0, NP, 128)
                                  : make_idesc(kFmtBF16, kFmtBF16, 0, NP, 128);
-      TileCursor tc;
-      tc.start(a.tile_off, a.B, g0);
+      ChunkWalker cw;
+      cw.start(a.tile_off, a.B, g0, g1, U);
       int cur_b = -1, seg = -1, it = 0;
-      for (int g = g0; g < g1; ++g, ++it) {
-        tc.advance(g);
-        const int b = tc.b;
+      int b, j0, n;
+      bool last;
+      for (; cw.next(b, j0, n, last); ++it) {
         if (b != cur_b) {
           if (seg >= 0) umma_commit(smem_u32(&qempty[seg & 1]));
           ++seg;
@@ -272,17 +298,19 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         const int acc = it % A;
         if (it >= A && !mbar_wait(smem_u32(&acce[acc]), ((it / A) - 1) & 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t a_base = smem_u32(kst + s * kTileBytes);
         const uint32_t b_base = smem_u32(qbuf + (seg & 1) * NP * 128);
-        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * NP);
+        for (int u = 0; u < n; ++u) {
+          const uint32_t a_base = smem_u32(kst + s * stage_bytes + u * kTileBytes);
+          const uint32_t d = tmem_base + static_cast<uint32_t>((acc * U + u) * NP);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = make_sdesc_sw128(a_base + kk * 32, 16, 1024);
-          const uint64_t bd = make_sdesc_sw128(b_base + kk * 32, 16, 1024);
-          if (FP8)
-            umma_f8(d, ad, bd, idesc, kk > 0);
-          else
-            umma_f16(d, ad, bd, idesc, kk > 0);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = make_sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = make_sdesc_sw128(b_base + kk * 32, 16, 1024);
+            if (FP8)
+              umma_f8(d, ad, bd, idesc, kk > 0);
+            else
+              umma_f16(d, ad, bd, idesc, kk > 0);
+          }
         }
         umma_commit(smem_u32(&empty[s]));
         umma_commit(smem_u32(&accf[acc]));
@@ -291,21 +319,83 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..9)
-    const int grp = (warp - 2) >> 2;         // tiles with it % 2 == grp
+    const int grp = (warp - 2) >> 2;         // chunks with it % 2 == grp
     const int quad = warp & 3;               // TMEM lanes 32*quad .. +31
-    const int row = quad * 32 + lane;        // token row of the tile
+    const int row = quad * 32 + lane;        // token row of each tile
     const int te = tid - 64;                 // 0..255
-    TileCursor tc;
-    tc.start(a.tile_off, a.B, g0);
+    ChunkWalker cw;
+    cw.start(a.tile_off, a.B, g0, g1, U);
     int cur_b = -1, seg = -1, it = 0;
     int Tcur = 0;
+    int b, j0, n;
+    bool last;
     bool ok = true;
-    // 64-column TMEM loads when no chunk straddles two ways
+    // 64-column TMEM loads when no chunk of columns straddles two ways
     const bool wide = (NP % 64 == 0) && (a.M == 1 || a.HI % 64 == 0);
-    for (int g = g0; g < g1 && ok; ++g, ++it) {
-      tc.advance(g);
-      const int b = tc.b;
-      const int j = g - tc.lo;
+    // sum_h w_h * ReLU(D[row][h]) of every way, from the NP columns at taddr;
+    // every product and partial sum is exact under the score contract, so
+    // four independent chains per chunk give the same result as one
+    auto head_sums = [&](uint32_t taddr, const float* wq, float* sm) {
+#pragma unroll
+      for (int m = 0; m < kMaxWays; ++m) sm[m] = 0.0f;
+      if (NP == 32) {
+        float v[32];
+        tmem_ld32(taddr, v);
+        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(wq + i);
+          p0 = fmaf(w4.x, fmaxf(v[i], 0.0f), p0);
+          p1 = fmaf(w4.y, fmaxf(v[i + 1], 0.0f), p1);
+          p2 = fmaf(w4.z, fmaxf(v[i + 2], 0.0f), p2);
+          p3 = fmaf(w4.w, fmaxf(v[i + 3], 0.0f), p3);
+        }
+        sm[0] = (p0 + p1) + (p2 + p3);
+      } else if (wide) {
+        for (int c = 0; c < NP / 64; ++c) {
+          float v[64];
+          tmem_ld64(taddr + c * 64, v);
+          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+          for (int i = 0; i < 64; i += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(wq + c * 64 + i);
+            p0 = fmaf(w4.x, fmaxf(v[i], 0.0f), p0);
+            p1 = fmaf(w4.y, fmaxf(v[i + 1], 0.0f), p1);
+            p2 = fmaf(w4.z, fmaxf(v[i + 2], 0.0f), p2);
+            p3 = fmaf(w4.w, fmaxf(v[i + 3], 0.0f), p3);
+          }
+          const float part = (p0 + p1) + (p2 + p3);
+          // columns c*64 .. belong to way c*64 / H_I (here H_I % 64 == 0 or M == 1)
+          const int m = (a.M == 1) ? 0 : (c * 64) / a.HI;
+          if (m == 0) sm[0] += part;
+          else if (m == 1) sm[1] += part;
+          else if (m == 2) sm[2] += part;
+          else sm[3] += part;
+        }
+      } else {
+        // 32-column chunks: a way of 32 heads, or N = 96 / 160 / 224
+        for (int c = 0; c < NP / 32; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(wq + c * 32 + i);
+            p0 = fmaf(w4.x, fmaxf(v[i], 0.0f), p0);
+            p1 = fmaf(w4.y, fmaxf(v[i + 1], 0.0f), p1);
+            p2 = fmaf(w4.z, fmaxf(v[i + 2], 0.0f), p2);
+            p3 = fmaf(w4.w, fmaxf(v[i + 3], 0.0f), p3);
+          }
+          const float part = (p0 + p1) + (p2 + p3);
+          const int m = (a.M == 1) ? 0 : (c * 32) / a.HI;   // H_I % 32 == 0 when M > 1
+          if (m == 0) sm[0] += part;
+          else if (m == 1) sm[1] += part;
+          else if (m == 2) sm[2] += part;
+          else sm[3] += part;
+        }
+      }
+    };
+    for (; ok && cw.next(b, j0, n, last); ++it) {
       if (b != cur_b) {
         ++seg;
         if (!mbar_wait(smem_u32(&qfull[seg & 1]), (seg >> 1) & 1, abort_flag)) break;
@@ -313,105 +403,47 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         Tcur = a.Tb[b];
       }
       if ((it & 1) == grp) {
-        // issue the scale load before waiting so its latency hides under the wait
-        const int t = j * kIdxTile + row;
-        const bool in_range = t < Tcur;
         const int acc = it % A;
         ok = mbar_wait(smem_u32(&accf[acc]), (it / A) & 1, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
         const float* wq = wbuf + (seg & 1) * NP;
-        float sm[kMaxWays];
+        // the head sums of the chunk's tiles (unrolled over kIdxSubMax so that
+        // they stay in registers)
+        float smv[kIdxSubMax][kMaxWays];
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
 #pragma unroll
-        for (int m = 0; m < kMaxWays; ++m) sm[m] = 0.0f;
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                               static_cast<uint32_t>(acc * NP);
-        // every product and partial sum is exact under the score contract, so
-        // four independent chains per chunk give the same result as one
-        if (NP == 32) {
-          float v[32];
-          tmem_ld32(taddr, v);
-          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 w4 = *reinterpret_cast<const float4*>(wq + i);
-            p0 = fmaf(w4.x, fmaxf(v[i], 0.0f), p0);
-            p1 = fmaf(w4.y, fmaxf(v[i + 1], 0.0f), p1);
-            p2 = fmaf(w4.z, fmaxf(v[i + 2], 0.0f), p2);
-            p3 = fmaf(w4.w, fmaxf(v[i + 3], 0.0f), p3);
-          }
-          sm[0] = (p0 + p1) + (p2 + p3);
-        } else if (wide) {
-          for (int c = 0; c < NP / 64; ++c) {
-            float v[64];
-            tmem_ld64(taddr + c * 64, v);
-            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-            for (int i = 0; i < 64; i += 4) {
-              const float4 w4 = *reinterpret_cast<const float4*>(wq + c * 64 + i);
-              p0 = fmaf(w4.x, fmaxf(v[i], 0.0f), p0);
-              p1 = fmaf(w4.y, fmaxf(v[i + 1], 0.0f), p1);
-              p2 = fmaf(w4.z, fmaxf(v[i + 2], 0.0f), p2);
-              p3 = fmaf(w4.w, fmaxf(v[i + 3], 0.0f), p3);
-            }
-            const float part = (p0 + p1) + (p2 + p3);
-            // columns n = c*64 + i belong to way n / H_I (here H_I % 64 == 0 or M == 1)
-            const int m = (a.M == 1) ? 0 : (c * 64) / a.HI;
-            if (m == 0) sm[0] += part;
-            else if (m == 1) sm[1] += part;
-            else if (m == 2) sm[2] += part;
-            else sm[3] += part;
-          }
-        } else {
-          // 32-column chunks: a way of 32 heads, or N = 96 / 160 / 224
-          for (int c = 0; c < NP / 32; ++c) {
-            float v[32];
-            tmem_ld32(taddr + c * 32, v);
-            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 w4 = *reinterpret_cast<const float4*>(wq + c * 32 + i);
-              p0 = fmaf(w4.x, fmaxf(v[i], 0.0f), p0);
-              p1 = fmaf(w4.y, fmaxf(v[i + 1], 0.0f), p1);
-              p2 = fmaf(w4.z, fmaxf(v[i + 2], 0.0f), p2);
-              p3 = fmaf(w4.w, fmaxf(v[i + 3], 0.0f), p3);
-            }
-            const float part = (p0 + p1) + (p2 + p3);
-            const int m = (a.M == 1) ? 0 : (c * 32) / a.HI;   // H_I % 32 == 0 when M > 1
-            if (m == 0) sm[0] += part;
-            else if (m == 1) sm[1] += part;
-            else if (m == 2) sm[2] += part;
-            else sm[3] += part;
-          }
-        }
+        for (int u = 0; u < kIdxSubMax; ++u)
+          if (u < n) head_sums(lane_base + static_cast<uint32_t>((acc * U + u) * NP), wq, smv[u]);
         tc_fence_before();
         mbar_arrive(smem_u32(&acce[acc]));
-        // the token's key scale, staged in shared memory with the tile
-        float sc = 1.0f;
+        // the tokens' key scales, staged in shared memory with the chunk
+        const int r = it % kScaleRing;
         if (a.scale != nullptr) {
-          const int r = it % kScaleRing;
-          if (in_range) {
-            ok = mbar_wait(smem_u32(&sfull[r]), (it / kScaleRing) & 1, abort_flag);
-            sc = sring[r * kIdxTile + row];
-          }
-          mbar_arrive(smem_u32(&sempty[r]));
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
+          bool any = false;
+          for (int u = 0; u < n; ++u) any |= (j0 + u) * kIdxTile + row < Tcur;
+          if (any) ok = mbar_wait(smem_u32(&sfull[r]), (it / kScaleRing) & 1, abort_flag);
         }
-        if (in_range) {
 #pragma unroll
-          for (int m = 0; m < kMaxWays; ++m) {   // unrolled: sm stays in registers
+        for (int u = 0; u < kIdxSubMax; ++u) {
+          const int t = (j0 + u) * kIdxTile + row;
+          if (u >= n || t >= Tcur) continue;
+          const float sc = a.scale != nullptr ? sring[(r * U + u) * kIdxTile + row] : 1.0f;
+#pragma unroll
+          for (int m = 0; m < kMaxWays; ++m) {   // unrolled: the sums stay in registers
             if (m >= a.M) break;
-            const float sv = __fmul_rn(sm[m], sc) + 0.0f;  // one rounding; +0 for a zero score
+            const float sv = __fmul_rn(smv[u][m], sc) + 0.0f;  // one rounding; +0 for zero
             a.scores[(static_cast<size_t>(b) * a.M + m) * a.T + t] = sv;
             if (HB) atomicAdd(hist + m * kHistBins + (float_key(sv) >> 20), 1u);
           }
         }
+        if (a.scale != nullptr) mbar_arrive(smem_u32(&sempty[r]));
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
       }
       // end of this request's run of tiles: release the query buffer and
       // publish the histogram once every epilogue thread has counted
-      const bool last = (g + 1 == g1) || (g + 1 >= tc.hi);
       if (last) {
         mbar_arrive(smem_u32(&qempty[seg & 1]));
         if (HB) {
@@ -441,26 +473,39 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   }
 }
 
-size_t indexer_smem_bytes(int S, int NP, int HB) {
-  return 1024 + static_cast<size_t>(S) * kTileBytes + 2u * NP * 128 + 2u * NP * 4 + HB * 4u +
-         (2 * S + 2 * kMaxAcc + 8 + 2 * kScaleRing) * 8 + kScaleRing * kIdxTile * 4 + 16;
+size_t indexer_smem_bytes(int S, int U, int NP, int HB) {
+  return 1024 + static_cast<size_t>(S) * U * kTileBytes + 2u * NP * 128 + 2u * NP * 4 +
+         HB * 4u + static_cast<size_t>(kScaleRing) * U * kIdxTile * 4 +
+         (2 * S + 2 * kMaxAcc + 8 + 2 * kScaleRing) * 8 + 16;
 }
 
-// Largest key ring (at most kIdxMaxStages) that fits one CTA beside the
-// queries, weights and histogram.
-int indexer_stages(int NP, int HB) {
-  int S = kIdxMaxStages;
-  while (S > kIdxMinStages && indexer_smem_bytes(S, NP, HB) > kMaxSmemPerCta) --S;
-  return S;
+// Tiles per chunk and key-ring stages for a query width: as many tiles per
+// chunk as keep U x N <= 256 TMEM columns (so at least two chunks' sums are
+// in flight), then as many stages as fit one CTA (at most kIdxMaxStages),
+// fewer tiles per chunk when not even kIdxMinStages stages fit.
+void indexer_shape(int NP, int HB, int* U_out, int* S_out) {
+  int U = 256 / NP < kIdxSubMax ? 256 / NP : kIdxSubMax;
+  if (U < 1) U = 1;
+  for (;; --U) {
+    int S = kIdxMaxStages;
+    while (S > kIdxMinStages && indexer_smem_bytes(S, U, NP, HB) > kMaxSmemPerCta) --S;
+    if (indexer_smem_bytes(S, U, NP, HB) <= kMaxSmemPerCta || U == 1) {
+      *U_out = U;
+      *S_out = S;
+      return;
+    }
+  }
 }
 
 }  // namespace
 
-// Shared memory of one indexer CTA with the fused score histogram and the
-// shortest ring (the kernel has no static shared memory).
+// Shared memory of one indexer CTA with the fused score histogram in its
+// smallest shape (the kernel has no static shared memory).
 size_t indexer_smem_need(const ess_config& c) {
   const int NP = ((c.mtp * c.idx_heads + 31) / 32) * 32;
-  return indexer_smem_bytes(kIdxMinStages, NP, c.mtp * kHistBins);
+  int U, S;
+  indexer_shape(NP, c.mtp * kHistBins, &U, &S);
+  return indexer_smem_bytes(S, U, NP, c.mtp * kHistBins);
 }
 
 cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, const float* w,
@@ -483,9 +528,9 @@ cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, cons
   a.NP = ((c.mtp * c.idx_heads + 31) / 32) * 32;
   a.T = c.max_T;
   a.total_tiles = L.total_tiles;
-  a.A = 512 / a.NP < kMaxAcc ? 512 / a.NP : kMaxAcc;
   const int HB = with_hist ? c.mtp * kHistBins : 0;
-  a.S = indexer_stages(a.NP, HB);
+  indexer_shape(a.NP, HB, &a.U, &a.S);
+  a.A = 512 / (a.U * a.NP) < kMaxAcc ? 512 / (a.U * a.NP) : kMaxAcc;
   a.early = L.append_pending ? 0 : 1;
   CUtensorMap qmap;
   if (!encode_map_2d(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_idx, kKeyRowBytes,
@@ -493,7 +538,7 @@ cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, cons
                      kKeyRowBytes, static_cast<uint32_t>(a.NP)))
     return cudaErrorInvalidValue;
   const int grid = L.total_tiles < p.num_sms ? L.total_tiles : p.num_sms;
-  const size_t smem = indexer_smem_bytes(a.S, a.NP, HB);
+  const size_t smem = indexer_smem_bytes(a.S, a.U, a.NP, HB);
   cudaError_t e;
   if (c.idx_dtype == ESS_FP8_E4M3) {
     e = cudaFuncSetAttribute(indexer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -26,7 +26,12 @@ constexpr int kHistBins = 4096;       // score histogram on the top 12 bits of t
 #define ESS_IDX_MAX_STAGES 6
 #endif
 constexpr int kIdxMaxStages = ESS_IDX_MAX_STAGES;
-constexpr int kIdxMinStages = 4;
+constexpr int kIdxMinStages = 2;
+// tiles per chunk: the indexer's barrier rounds move up to this many 128-token tiles
+#ifndef ESS_IDX_SUB
+#define ESS_IDX_SUB 4
+#endif
+constexpr int kIdxSubMax = ESS_IDX_SUB;
 constexpr int kIdxTile = 128;         // tokens per tile (MMA M)
 
 constexpr int kSelCluster = 8;        // CTAs per request in the selection kernel
