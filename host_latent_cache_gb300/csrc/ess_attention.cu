@@ -37,6 +37,8 @@ constexpr uint32_t kBlk = 16384;         // one [128 rows x 64 dims] bf16 block
 constexpr int kDimBlocks = kRowDim / 64; // 9
 constexpr uint32_t kRowsBytes = kDimBlocks * kBlk;   // 147456
 constexpr uint32_t kQBytes = QST * kBlk;             // 65536
+constexpr int kMergeBatch = 4;       // chunk partials in flight per merge thread
+constexpr int kMergeMinBlocks = 12;  // merge CTAs per SM the register budget allows
 
 struct AttnArgs {
   const int32_t* topk_idx;    // [B][M][k]
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       set_status(a.status, ESS_ERR_DEVICE_CHECK);
       valid = false;
     } else if (miss && !a.staged && a.compact) {
-      cmiss = true;
+      cmiss = true;   // widened below
       src = reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(a.host) +
                                               (static_cast<size_t>(b) * a.T + prow) *
                                                   kCompactRowBytes);
@@ -389,12 +391,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // out[b][m][h][:] = sum_c 2^(mx_c - M) O_c[h][:] / sum_c 2^(mx_c - M) l_c over the
-// chunk partials of (request b, way m), M the running maximum (merged 16
-// chunks at a time, rescaling the running sums when M grows).  One CTA per
-// (head, request-way); thread t owns dims 4t..4t+3.  Launched as a
+// chunk partials of (request b, way m), M the running maximum (merged
+// kMergeBatch chunks at a time, rescaling the running sums when M grows).  One
+// CTA per (head, request-way); thread t owns dims 4t..4t+3.  Launched as a
 // programmatic dependent of the attention kernel: it waits for that grid
-// before reading the partials.
-__global__ void __launch_bounds__(128) merge_kernel(const uint16_t* __restrict__ part_o,
+// before reading the partials.  Few registers per thread, so that every CTA
+// is resident at once beside the attention CTAs (a second wave would add its
+// whole latency to the step).
+__global__ void __launch_bounds__(128, kMergeMinBlocks) merge_kernel(const uint16_t* __restrict__ part_o,
                                                     const float2* __restrict__ part_ml,
                                                     float* __restrict__ out, int H, int nch) {
   pdl_wait_previous();
@@ -408,18 +412,18 @@ __global__ void __launch_bounds__(128) merge_kernel(const uint16_t* __restrict__
   const size_t cstride = static_cast<size_t>(H) * (kLatent / 4);   // one chunk, in uint2 units
   float M = -INFINITY, L = 0.0f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = 0; c0 < nch; c0 += 16) {
-    float2 e[16];
-    uint2 v[16];
+  for (int c0 = 0; c0 < nch; c0 += kMergeBatch) {
+    float2 e[kMergeBatch];
+    uint2 v[kMergeBatch];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
+    for (int q = 0; q < kMergeBatch; ++q) {
       const int c = c0 + q;
       e[q] = c < nch ? __ldg(ml + static_cast<size_t>(c) * H) : make_float2(-INFINITY, 0.0f);
       v[q] = c < nch ? __ldg(po + static_cast<size_t>(c) * cstride) : make_uint2(0u, 0u);
     }
     float Mg = M;
 #pragma unroll
-    for (int q = 0; q < 16; ++q)
+    for (int q = 0; q < kMergeBatch; ++q)
       if (e[q].y > 0.0f) Mg = fmaxf(Mg, e[q].x);
     const float r = (M == -INFINITY) ? 0.0f : exp2f(M - Mg);
     acc.x *= r;
@@ -428,7 +432,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const uint16_t* __restrict__
     acc.w *= r;
     L *= r;
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
+    for (int q = 0; q < kMergeBatch; ++q) {
       if (e[q].y > 0.0f) {   // a chunk with no rows leaves no O partial
         const float w = exp2f(e[q].x - Mg);
         const float2 lo = half2_bits_to_float2(v[q].x), hi = half2_bits_to_float2(v[q].y);
