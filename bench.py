@@ -65,6 +65,9 @@ def parse():
                          "scales + bf16 RoPE), widened to bf16 on the way in")
     ap.add_argument("--empty-pool", action="store_true",
                     help="time from an empty pool instead of filling it first")
+    ap.add_argument("--prime-random", action="store_true",
+                    help="start from a full pool of random resident tokens instead of filling it "
+                         "by decode steps (short runs, e.g. under a profiler)")
     ap.add_argument("--cpu-steps", type=int, default=48)
     ap.add_argument("--overlap-steps", type=int, default=24)
     ap.add_argument("--pipeline", type=int, default=0,
@@ -583,8 +586,15 @@ def bench_ours(args, cfg, rank, world, local_rank):
     wts = W.head_weights(cfg_r, ld.w)
     stream = torch.cuda.current_stream()
     # steady state: the pool is filled by real decode steps before the warm-up
-    fill_steps, occupancy = (fill_pool(sess, qs, wts, stream) if not args.empty_pool
-                             else (0, 0.0))
+    if args.prime_random:
+        # a full pool of random resident tokens (short runs, e.g. under a profiler):
+        # the warm-up steps then settle it into the queries' working set
+        sess.set_state(0, W.full_pool_state(cfg_r, ld, 0, age=8))
+        fill_steps, occupancy = 0, 1.0
+    elif args.empty_pool:
+        fill_steps, occupancy = 0, 0.0
+    else:
+        fill_steps, occupancy = fill_pool(sess, qs, wts, stream)
     dev_inputs, host_inputs = [], []
     for s in range(n_total):
         q, enc, qm = qs.next()
@@ -724,8 +734,10 @@ def bench_ours(args, cfg, rank, world, local_rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
             "config": dict(config_json(cfg, world, args.miss_mode),
                            pool_fill_steps=fill_steps, pool_occupancy_at_warmup=occupancy,
-                           pool_state="steady (full before the warm-up)" if occupancy >= 1.0
-                           else "filling"),
+                           pool_state=("full of random tokens before the warm-up"
+                                       if args.prime_random else
+                                       "steady (full before the warm-up)" if occupancy >= 1.0
+                                       else "filling")),
             "roofline": {"bound": "hbm", "kernel": "indexer (a1)", "achieved": achieved,
                          "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                          "traffic": traffic, "peak_source": peak_src,
