@@ -54,7 +54,7 @@ Layout compute_layout(const ess_config& c) {
   L.o_T = o;        o = align256(o + B * 4);
   L.o_tiles = o;    o = align256(o + (B + 1) * 4);
   L.o_step = o;     o = align256(o + B * 4);
-  L.o_stats = o;    o = align256(o + 8 * 8);
+  L.o_stats = o;    o = align256(o + kStatFields * 8);
   L.o_cslots = o;   o = align256(o + B * T * 4);
   L.o_stoken = o;   o = align256(o + B * C * 4);
   L.o_lused = o;    o = align256(o + B * C * 4);
@@ -62,6 +62,7 @@ Layout compute_layout(const ess_config& c) {
   L.o_pool = o;     o = align256(o + B * C * kRowBytes);
   L.o_T0 = o;       o = align256(o + B * 4);
   L.o_tail = o;     o = align256(o + B * 2 * c.page * kRowBytes);
+  L.o_guess = o;    o = align256(o + B * M * 4);
   L.layer_bytes = o;
   o = L.layer_bytes * c.n_layers;
   L.o_scores = o;   o = align256(o + B * M * T * 4);
@@ -80,6 +81,8 @@ Layout compute_layout(const ess_config& c) {
   L.o_hqm = o;      o = align256(o + B * M * H * kRowBytes);
   L.o_hout = o;     o = align256(o + B * M * H * kLatent * 4);
   L.o_status = o;   o = align256(o + 256);
+  L.o_fhist = o;    o = align256(o + B * M * kFineBins * 4);
+  L.o_tflag = o;    o = align256(o + B * M * ((T + 31) / 32) * 4);
   L.total = o;
   return L;
 }
@@ -157,8 +160,10 @@ cudaError_t launch_reset(const ess_pool& p, int layer, cudaStream_t st) {
   if ((e = cudaMemsetAsync(L.last_used, 0xff, B * c.C * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(L.step, 0, B * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(p.scr.ghist, 0, B * c.mtp * kHistBins * 4, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(p.scr.fhist, 0, B * c.mtp * kFineBins * 4, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(L.guess, 0, B * c.mtp * 4, st)) != cudaSuccess) return e;
   if ((e = launch_order_reset(p, layer, st)) != cudaSuccess) return e;
-  return cudaMemsetAsync(L.stats, 0, 8 * 8, st);
+  return cudaMemsetAsync(L.stats, 0, kStatFields * 8, st);
 }
 
 }  // namespace ess
@@ -252,6 +257,7 @@ ess_status ess_pool_create(const ess_config* cfg, void* dev_workspace, size_t ws
     y.pool = reinterpret_cast<uint16_t*>(base + L.o_pool);
     y.T0_dev = reinterpret_cast<int32_t*>(base + L.o_T0);
     y.tail = reinterpret_cast<uint16_t*>(base + L.o_tail);
+    y.guess = reinterpret_cast<uint32_t*>(base + L.o_guess);
   }
   Scratch& r = p->scr;
   r.scores = reinterpret_cast<float*>(p->ws + L.o_scores);
@@ -270,6 +276,9 @@ ess_status ess_pool_create(const ess_config* cfg, void* dev_workspace, size_t ws
   r.h_qmla = reinterpret_cast<uint16_t*>(p->ws + L.o_hqm);
   r.h_out = reinterpret_cast<float*>(p->ws + L.o_hout);
   r.status = reinterpret_cast<int32_t*>(p->ws + L.o_status);
+  r.fhist = reinterpret_cast<uint32_t*>(p->ws + L.o_fhist);
+  r.tflag = reinterpret_cast<uint32_t*>(p->ws + L.o_tflag);
+  r.nwords = (cfg->max_T + 31) / 32;
   cudaError_t e = cudaSuccess;
   for (int l = 0; l < cfg->n_layers && e == cudaSuccess; ++l) {
     e = launch_reset(*p, l, nullptr);
@@ -648,6 +657,8 @@ ess_status ess_pool_read_stats(ess_pool* pool, int layer, ess_stats* out, int re
   out->union_size = v[3];
   out->miss_rows = v[4];
   out->miss_bytes = v[5];
+  out->guided = v[6];
+  out->fine_cuts = v[7];
   if (reset && cudaMemset(L.stats, 0, sizeof(v)) != cudaSuccess) return ESS_ERR_CUDA;
   return ESS_OK;
 }

@@ -24,7 +24,12 @@
 //              in a shared-memory histogram of the top 12 bits of its ordered
 //              key, which is added to a per-(request, way) global histogram
 //              at the end of each request's run of tiles (one histogram per
-//              way, flushed and cleared between two barriers).
+//              way, flushed and cleared between two barriers).  Given a
+//              guessed coarse bin g per (request, way), it also sets the
+//              token's bit in a flag bitmap when its key lies in bin g or
+//              above (one ballot per 32 tokens) and counts keys of bins
+//              g .. g + 3 in a fine histogram on 8 more bits, so that the
+//              selection can skip the tokens far below the cut.
 // The key tiles are the only large HBM stream; the kernel is bound by HBM
 // bandwidth (about 132 B per token and request).
 #include "ess_device.cuh"
@@ -40,6 +45,10 @@ struct IdxArgs {
   const uint8_t* q;          // [B][M][H_I][128 B]
   float* scores;             // [B][M][T]
   uint32_t* ghist;           // [B][M][kHistBins] or null
+  const uint32_t* guess;     // [B][M] guessed coarse bin (0: none), or null
+  uint32_t* fhist;           // [B][M][kFineBins] (with guess)
+  uint32_t* tflag;           // [B][M][nwords] (with guess)
+  int nwords;
   int* status;
   int B, M, HI, NP, T, total_tiles, A;
   int S;                     // key-ring stages (chunks)
@@ -99,7 +108,9 @@ struct ChunkWalker {
   }
 };
 
-template <bool FP8>
+// MW: the number of ways, fixed at compile time so that the epilogue's
+// per-way code unrolls to exactly the ways that exist
+template <bool FP8, int MW>
 __global__ void __launch_bounds__(kIdxThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                    const IdxArgs a) {
@@ -115,7 +126,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   uint8_t* qbuf = kst + S * stage_bytes;                 // 2 x NP x 128 B queries
   float* wbuf = reinterpret_cast<float*>(qbuf + 2 * NP * 128);  // 2 x NP weights
   uint32_t* hist = reinterpret_cast<uint32_t*>(wbuf + 2 * NP);   // M x kHistBins
-  const int HB = a.ghist ? a.M * kHistBins : 0;
+  // the fine histograms follow the coarse ones: M x kFineBins
+  const int HC = a.ghist ? a.M * kHistBins : 0;
+  const int HB = HC + (a.ghist && a.guess ? a.M * kFineBins : 0);
   float* sring = reinterpret_cast<float*>(hist + HB);   // [kScaleRing][U x 128] key scales
   uint64_t* bars = reinterpret_cast<uint64_t*>(sring + kScaleRing * U * kIdxTile);
   uint64_t* full = bars;
@@ -327,11 +340,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     cw.start(a.tile_off, a.B, g0, g1, U);
     int cur_b = -1, seg = -1, it = 0;
     int Tcur = 0;
+    uint32_t gm[kMaxWays] = {0u, 0u, 0u, 0u};   // guessed coarse bin per way (0: none)
     int b, j0, n;
     bool last;
     bool ok = true;
     // 64-column TMEM loads when no chunk of columns straddles two ways
-    const bool wide = (NP % 64 == 0) && (a.M == 1 || a.HI % 64 == 0);
+    const bool wide = (NP % 64 == 0) && (MW == 1 || a.HI % 64 == 0);
     // sum_h w_h * ReLU(D[row][h]) of every way, from the NP columns at taddr;
     // every product and partial sum is exact under the score contract, so
     // four independent chains per chunk give the same result as one
@@ -366,7 +380,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           }
           const float part = (p0 + p1) + (p2 + p3);
           // columns c*64 .. belong to way c*64 / H_I (here H_I % 64 == 0 or M == 1)
-          const int m = (a.M == 1) ? 0 : (c * 64) / a.HI;
+          const int m = (MW == 1) ? 0 : (c * 64) / a.HI;
           if (m == 0) sm[0] += part;
           else if (m == 1) sm[1] += part;
           else if (m == 2) sm[2] += part;
@@ -387,7 +401,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             p3 = fmaf(w4.w, fmaxf(v[i + 3], 0.0f), p3);
           }
           const float part = (p0 + p1) + (p2 + p3);
-          const int m = (a.M == 1) ? 0 : (c * 32) / a.HI;   // H_I % 32 == 0 when M > 1
+          const int m = (MW == 1) ? 0 : (c * 32) / a.HI;   // H_I % 32 == 0 when M > 1
           if (m == 0) sm[0] += part;
           else if (m == 1) sm[1] += part;
           else if (m == 2) sm[2] += part;
@@ -401,6 +415,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (!mbar_wait(smem_u32(&qfull[seg & 1]), (seg >> 1) & 1, abort_flag)) break;
         cur_b = b;
         Tcur = a.Tb[b];
+#pragma unroll
+        for (int m = 0; m < kMaxWays; ++m)
+          gm[m] = (HB > HC && m < MW) ? a.guess[b * MW + m] : 0u;
       }
       if ((it & 1) == grp) {
         const int acc = it % A;
@@ -427,15 +444,31 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         }
 #pragma unroll
         for (int u = 0; u < kIdxSubMax; ++u) {
+          if (u >= n) continue;   // the same in every lane
           const int t = (j0 + u) * kIdxTile + row;
-          if (u >= n || t >= Tcur) continue;
-          const float sc = a.scale != nullptr ? sring[(r * U + u) * kIdxTile + row] : 1.0f;
+          const bool valid = t < Tcur;
+          const float sc =
+              (valid && a.scale != nullptr) ? sring[(r * U + u) * kIdxTile + row] : 1.0f;
+          const int word = (j0 + u) * (kIdxTile / 32) + quad;   // this warp's 32 tokens
 #pragma unroll
           for (int m = 0; m < kMaxWays; ++m) {   // unrolled: the sums stay in registers
-            if (m >= a.M) break;
-            const float sv = __fmul_rn(smv[u][m], sc) + 0.0f;  // one rounding; +0 for zero
-            a.scores[(static_cast<size_t>(b) * a.M + m) * a.T + t] = sv;
-            if (HB) atomicAdd(hist + m * kHistBins + (float_key(sv) >> 20), 1u);
+            if (m >= MW) break;
+            uint32_t key = 0u;
+            if (valid) {
+              const float sv = __fmul_rn(smv[u][m], sc) + 0.0f;  // one rounding; +0 for zero
+              a.scores[(static_cast<size_t>(b) * a.M + m) * a.T + t] = sv;
+              key = float_key(sv);
+              if (HB) atomicAdd(hist + m * kHistBins + (key >> 20), 1u);
+              const uint32_t d = (key >> 20) - gm[m];
+              if (gm[m] != 0u && d < static_cast<uint32_t>(kFineWin))
+                atomicAdd(hist + HC + m * kFineBins + d * kFineSub + ((key >> 12) & (kFineSub - 1)),
+                          1u);
+            }
+            if (gm[m] != 0u) {   // the same in every lane
+              const unsigned f = __ballot_sync(0xffffffffu, valid && (key >> 20) >= gm[m]);
+              if (lane == 0 && word < a.nwords)
+                a.tflag[(static_cast<size_t>(b) * a.M + m) * a.nwords + word] = f;
+            }
           }
         }
         if (a.scale != nullptr) mbar_arrive(smem_u32(&sempty[r]));
@@ -450,10 +483,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           mbar_arrive(smem_u32(&epdone[seg & 1]));
           if (!mbar_wait(smem_u32(&epdone[seg & 1]), (seg >> 1) & 1, abort_flag)) break;
           uint32_t* gh = a.ghist + static_cast<size_t>(b) * a.M * kHistBins;
+          uint32_t* gf = HB > HC ? a.fhist + static_cast<size_t>(b) * a.M * kFineBins : nullptr;
           for (int i = te; i < HB; i += 256) {
             const uint32_t v = hist[i];
             if (v) {
-              atomicAdd(gh + i, v);
+              atomicAdd(i < HC ? gh + i : gf + (i - HC), v);
               hist[i] = 0;
             }
           }
@@ -503,9 +537,10 @@ void indexer_shape(int NP, int HB, int* U_out, int* S_out) {
 // smallest shape (the kernel has no static shared memory).
 size_t indexer_smem_need(const ess_config& c) {
   const int NP = ((c.mtp * c.idx_heads + 31) / 32) * 32;
+  const int HB = c.mtp * (kHistBins + kFineBins);
   int U, S;
-  indexer_shape(NP, c.mtp * kHistBins, &U, &S);
-  return indexer_smem_bytes(S, U, NP, c.mtp * kHistBins);
+  indexer_shape(NP, HB, &U, &S);
+  return indexer_smem_bytes(S, U, NP, HB);
 }
 
 cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, const float* w,
@@ -521,6 +556,12 @@ cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, cons
   a.q = static_cast<const uint8_t*>(q_idx);
   a.scores = scores;
   a.ghist = with_hist ? p.scr.ghist : nullptr;
+  // the flags and the fine histogram go with the histogram: the selection
+  // that reads it follows on the stream and keeps the guesses
+  a.guess = with_hist ? L.guess : nullptr;
+  a.fhist = p.scr.fhist;
+  a.tflag = p.scr.tflag;
+  a.nwords = p.scr.nwords;
   a.status = p.scr.status;
   a.B = c.batch;
   a.M = c.mtp;
@@ -528,7 +569,7 @@ cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, cons
   a.NP = ((c.mtp * c.idx_heads + 31) / 32) * 32;
   a.T = c.max_T;
   a.total_tiles = L.total_tiles;
-  const int HB = with_hist ? c.mtp * kHistBins : 0;
+  const int HB = with_hist ? c.mtp * (kHistBins + kFineBins) : 0;
   indexer_shape(a.NP, HB, &a.U, &a.S);
   a.A = 512 / (a.U * a.NP) < kMaxAcc ? 512 / (a.U * a.NP) : kMaxAcc;
   a.early = L.append_pending ? 0 : 1;
@@ -540,17 +581,16 @@ cudaError_t launch_indexer(const ess_pool& p, int layer, const void* q_idx, cons
   const int grid = L.total_tiles < p.num_sms ? L.total_tiles : p.num_sms;
   const size_t smem = indexer_smem_bytes(a.S, a.U, a.NP, HB);
   cudaError_t e;
-  if (c.idx_dtype == ESS_FP8_E4M3) {
-    e = cudaFuncSetAttribute(indexer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(indexer_kernel<true>, dim3(grid), dim3(kIdxThreads), smem, st, L.kmap, qmap, a);
-  } else {
-    e = cudaFuncSetAttribute(indexer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(indexer_kernel<false>, dim3(grid), dim3(kIdxThreads), smem, st, L.kmap, qmap, a);
-  }
+  using Kern = void (*)(CUtensorMap, CUtensorMap, IdxArgs);
+  static const Kern kern_fp8[kMaxWays] = {indexer_kernel<true, 1>, indexer_kernel<true, 2>,
+                                          indexer_kernel<true, 3>, indexer_kernel<true, 4>};
+  static const Kern kern_bf16[kMaxWays] = {indexer_kernel<false, 1>, indexer_kernel<false, 2>,
+                                           indexer_kernel<false, 3>, indexer_kernel<false, 4>};
+  const Kern kern = (c.idx_dtype == ESS_FP8_E4M3 ? kern_fp8 : kern_bf16)[c.mtp - 1];
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(kern, dim3(grid), dim3(kIdxThreads), smem, st, L.kmap, qmap, a);
   if (e == cudaSuccess) {
     count_launch(p);
     // this launch waits for any append before it, so the next one may load early

@@ -21,6 +21,12 @@ constexpr int kKeyRowBytes = 128;     // one indexer key row
 
 constexpr int kIdxThreads = 320;      // 10 warps: TMA, MMA, 2 groups of 4 epilogue warps
 constexpr int kHistBins = 4096;       // score histogram on the top 12 bits of the ordered key
+// Guided selection: the indexer also flags every token whose key lies at or
+// above a guessed coarse bin g (the previous step's threshold bin less one)
+// and counts the keys of bins g .. g + kFineWin - 1 on 8 more bits.
+constexpr int kFineWin = 4;           // coarse bins covered by the fine histogram
+constexpr int kFineSub = 256;         // fine bins per coarse bin
+constexpr int kFineBins = kFineWin * kFineSub;
 // key-tile ring: as many 16 KB stages as fit one CTA, up to kIdxMaxStages
 #ifndef ESS_IDX_MAX_STAGES
 #define ESS_IDX_MAX_STAGES 6
@@ -41,7 +47,7 @@ constexpr int kAttnRows = 128;        // selected rows per attention CTA
 constexpr int kAttnThreads = 128;
 constexpr int kAttnQStages = 4;
 
-constexpr int kStatFields = 6;        // ess_stats fields kept on the device
+constexpr int kStatFields = 8;        // ess_stats fields kept on the device
 
 // Bindings and state of one layer (device pointers point into the workspace
 // or at caller buffers).
@@ -72,6 +78,7 @@ struct Layer {
   int32_t* last_used = nullptr;   // [B][C]
   int32_t* step = nullptr;        // [B]
   int32_t* order = nullptr;       // [2][B][C] slots in (last_used, slot) order, by step parity
+  uint32_t* guess = nullptr;      // [B][M] coarse bin the next indexer flags from (0: none)
   uint16_t* pool = nullptr;       // [B][C][D] bf16
   long long* stats = nullptr;     // [kStatFields]
 };
@@ -86,6 +93,9 @@ struct Scratch {
   int32_t* n_miss = nullptr;      // [B]
   int32_t* vlist = nullptr;       // [B][M*k] victims in LRU order
   uint32_t* ghist = nullptr;      // [B][M][kHistBins] score histogram
+  uint32_t* fhist = nullptr;      // [B][M][kFineBins] fine histogram over the guessed window
+  uint32_t* tflag = nullptr;      // [B][M][nwords] bit t % 32 of word t / 32: key >= guess
+  int nwords = 0;                 // flag words per (request, way): ceil(max_T / 32)
   uint16_t* part_o = nullptr;     // [B][M][nch][H][512] fp16, 16-byte units XOR-swizzled by head
   float2* part_ml = nullptr;      // [B][M][nch][H]
   uint8_t* h_qidx = nullptr;      // staging for ess_step_host
@@ -101,10 +111,10 @@ struct Layout {
   size_t layer_bytes = 0;
   // per layer (relative to the layer base)
   size_t o_T, o_tiles, o_cslots, o_stoken, o_lused, o_step, o_pool, o_stats, o_order, o_T0,
-      o_tail;
+      o_tail, o_guess;
   // scratch (absolute)
   size_t o_scores, o_tidx, o_tslot, o_nmw, o_mtok, o_mslot, o_nmiss, o_vict, o_hist, o_po, o_pml,
-      o_hq, o_hw, o_hqm, o_hout, o_status;
+      o_hq, o_hw, o_hqm, o_hout, o_status, o_fhist, o_tflag;
   int nch = 0;                    // attention chunks per (request, way)
 };
 

@@ -54,11 +54,19 @@ constexpr int NW = NT / 32;
 
 constexpr int kDigBits = 10;               // radix digit width of the exact passes
 constexpr int kDig = 1 << kDigBits;
+constexpr int kDirectRank = 128;           // gathered candidates ranked one against another
 
 struct SelArgs {
   const float* scores;        // [B][M][T]
   uint32_t* ghist;            // [B][M][kHistBins]
   int hist_given;             // 1: filled by the indexer; 0: build it here
+  // guided selection (with the indexer's histogram only): the coarse bin the
+  // indexer flagged from per (request, way), rewritten here for the next step;
+  // the indexer's fine histogram and flag bitmap
+  uint32_t* guess;            // [B][M] or null
+  uint32_t* fhist;            // [B][M][kFineBins]
+  const uint32_t* tflag;      // [B][M][nwords]
+  int nwords;
   int32_t* cache_slots;       // [B][T]
   int32_t* slot_token;        // [B][C]
   int32_t* last_used;         // [B][C]
@@ -102,6 +110,8 @@ struct SelShared {
   int active[kMaxWays], quota[kMaxWays], rank_needed[kMaxWays];
   int last_lo, last_dmask;
   int b1[kMaxWays], take1[kMaxWays], cand1[kMaxWays];  // coarse threshold bin per way
+  uint32_t g[kMaxWays];               // guessed coarse bin the indexer flagged from (0: none)
+  int fine[kMaxWays], fb[kMaxWays];   // the cut's fine bin within b1, when the fine histogram has it
   int fallback;
   int nl;
   int ncand[kMaxWays];                // this CTA's candidates per way (read through DSMEM)
@@ -348,6 +358,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     for (int m = 0; m < kMaxWays; ++m) {
       sh.pub_hit[m] = sh.pub_miss[m] = 0;
       sh.active[m] = 0;
+      sh.g[m] = (a.guess != nullptr && m < M) ? a.guess[b * M + m] : 0u;
+      sh.fine[m] = 0;
     }
     mbar_init(smem_u32(&sh.bar), 1);
     fence_mbar_init();
@@ -443,6 +455,65 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     __syncthreads();
   }
   bool fast = !sel_all && !sh.fallback;
+  const bool have_b1 = fast;   // the coarse bins describe this step's scores
+  // Guided: every way's threshold bin lies at or above the bin its flags start
+  // from, so the flagged tokens hold the whole selection and its candidates.
+  bool guided = fast && a.tflag != nullptr;
+  for (int m = 0; m < M; ++m)
+    guided = guided && sh.g[m] != 0u && static_cast<uint32_t>(sh.b1[m]) >= sh.g[m];
+  if (guided) {
+    // a way whose threshold bin the fine histogram covers takes its cut on 8
+    // more key bits: candidates are the keys of one fine bin
+    if (warp < M) {
+      const int m = warp;
+      const uint32_t d = static_cast<uint32_t>(sh.b1[m]) - sh.g[m];
+      int fine = 0;
+      if (d < static_cast<uint32_t>(kFineWin)) {
+        const uint32_t* F = a.fhist + (static_cast<size_t>(b) * M + m) * kFineBins + d * kFineSub;
+        // lane l owns fine bins 255 - 8l - j, j = 0..7 (descending)
+        int c8[8];
+        int s8 = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c8[j] = static_cast<int>(F[kFineSub - 1 - 8 * lane - j]);
+          s8 += c8[j];
+        }
+        int incl = s8;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int tot = __shfl_sync(0xffffffffu, incl, 31);
+        const int need = sh.take1[m];
+        if (tot == sh.cand1[m]) {   // the fine bins add up to the coarse bin
+          fine = 1;
+          const unsigned bal = __ballot_sync(0xffffffffu, incl >= need);
+          if (lane == __ffs(bal) - 1) {
+            int acc = incl - s8, jsel = 7, cj = c8[7];
+            bool found = false;
+#pragma unroll
+            for (int j = 0; j < 7; ++j) {
+              if (!found) {
+                if (acc + c8[j] >= need) {
+                  found = true;
+                  jsel = j;
+                  cj = c8[j];
+                } else {
+                  acc += c8[j];
+                }
+              }
+            }
+            sh.fb[m] = kFineSub - 1 - 8 * lane - jsel;
+            sh.take1[m] = need - acc;
+            sh.cand1[m] = cj;
+          }
+        }
+      }
+      if (lane == 0) sh.fine[m] = fine;
+    }
+    __syncthreads();
+  }
   if (sel_all) {
     for (int i = tid; i < nloc; i += NT) {
       ltok[i] = r0 + i;
@@ -461,6 +532,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       const bool use = m < M;
       const uint32_t bin = use ? static_cast<uint32_t>(sh.b1[m]) : 0xFFFu;
       const bool all_in = use && sh.take1[m] == sh.cand1[m];
+      if (use && sh.fine[m]) {
+        // the cut's fine bin: 4096 keys wide
+        const uint32_t lo = (bin << 20) | (static_cast<uint32_t>(sh.fb[m]) << 12);
+        lo_k[m] = lo;
+        hi_k[m] = all_in ? lo : (lo == 0xFFFFF000u ? 0xFFFFFFFFu : lo + 4096u);
+        continue;
+      }
       lo_k[m] = bin << 20;                                    // key >= lo: at or above the bin
       hi_k[m] = all_in ? (bin << 20) : ((bin + 1u) << 20);    // key >= hi: selected outright
       if (!use) lo_k[m] = hi_k[m] = 0xFFFFFFFFu;
@@ -477,6 +555,43 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       }
       return f;
     };
+    int total;
+    if (guided) {
+      // the flagged tokens only: one flag word per thread (the ways' words
+      // OR-ed, clipped to this CTA's tokens); its tokens that the keys place
+      // at or above the cut are counted, given ordered positions, and listed
+      const int w0 = r0 >> 5, w1 = (r0 + nloc + 31) >> 5;
+      int run = 0;
+      for (int wb = w0; wb < w1; wb += NT) {
+        const int w = wb + tid;
+        uint32_t bits = 0u;
+        if (w < w1 && nloc > 0) {
+#pragma unroll
+          for (int m = 0; m < kMaxWays; ++m) {
+            if (m >= M) break;
+            bits |= a.tflag[(static_cast<size_t>(b) * M + m) * a.nwords + w];
+          }
+          const int tlo = w * 32, thi = r0 + nloc;
+          if (tlo < r0) bits &= 0xFFFFFFFFu << (r0 - tlo);
+          if (thi - tlo < 32) bits &= (1u << (thi - tlo)) - 1u;
+        }
+        uint32_t q = 0u;
+        for (uint32_t x = bits; x != 0u; x &= x - 1u) {
+          const int j = __ffs(x) - 1;
+          if (coarse_flags(w * 32 + j - r0)) q |= 1u << j;
+        }
+        int p = ordered_pos(__popc(q), run, sh, parity);
+        for (uint32_t x = q; x != 0u; x &= x - 1u) {
+          const int i = w * 32 + (__ffs(x) - 1) - r0;
+          if (p < lcap) {
+            ltok[p] = r0 + i;
+            lflag[p] = static_cast<uint8_t>(coarse_flags(i));
+          }
+          ++p;
+        }
+      }
+      total = run;
+    } else {
     const int per_w = (((nloc + NW - 1) / NW) + 31) & ~31;
     const int wlo = warp * per_w;
     const int whi = wlo + per_w < nloc ? wlo + per_w : nloc;
@@ -514,7 +629,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       }
     }
     __syncwarp();
-    int total;
     int pos = warp_base(wcnt, total, sh);
     if (wcnt <= WSTAGE) {
       for (int j = lane; j < wcnt; j += 32) {
@@ -538,6 +652,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         }
         pos += __popc(bal);
       }
+    }
     }
     const int nl = total < lcap ? total : lcap;
     // candidates of each way in list order, with their low 20 key bits
@@ -594,6 +709,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         for (int r = 0; r < CL; ++r) roff[r + 1] = roff[r] + sh.gcnt[r];
         const int off = roff[CL];
         const int ngc = off < a.gcap ? off : a.gcap;
+        const int need0 = sh.remaining[m];   // unchanged until after the next barrier
         const uint32_t kbase = smem_u32(ckey + m * lcap);
         for (int g = tid; g < ngc; g += NT) {
           int r = 0;
@@ -607,9 +723,29 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         }
         __syncthreads();
         const int ng = off < a.gcap ? off : a.gcap;
+        uint32_t pre = 0;
+        if (ng <= kDirectRank) {
+          // few candidates: each one's rank among them (equal keys by their
+          // place in cluster order, i.e. by token); rank need - 1 is the cut
+          if (tid < ng) {
+            const uint32_t kg = gkey[tid];
+            int gt = 0, eqb = 0;
+            for (int i = 0; i < ng; ++i) {
+              const uint32_t ki = gkey[i];
+              gt += ki > kg ? 1 : 0;
+              eqb += (ki == kg && i < tid) ? 1 : 0;
+            }
+            if (gt + eqb == need0 - 1) {
+              sh.prefix[m] = kg;
+              sh.remaining[m] = need0 - gt;   // threshold-equal candidates to take
+            }
+          }
+          __syncthreads();
+          pre = sh.prefix[m];
+        } else {
         // exact take1-th largest of the gathered keys: two 10-bit passes
         uint32_t* H = sh.hist[0];
-        uint32_t pre = 0, msk = 0;
+        uint32_t msk = 0;
         int need = sh.remaining[m];
         for (int p = 0; p < 2; ++p) {
           const int lo = p == 0 ? 10 : 0;
@@ -639,6 +775,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
           msk |= static_cast<uint32_t>(kDig - 1) << lo;
           need = sh.remaining[m];
           __syncthreads();
+        }
         }
         // threshold-equal candidates: this CTA's count and those of lower ranks
         if (tid == 0) {
@@ -797,18 +934,21 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   if (tid == 0) sh.pub_nu = nu;
   __syncthreads();
   cluster_sync();  // [S3] stamps visible, per-CTA counts published
+  // the cluster sums, each in a warp of its own so that their remote reads overlap
   if (tid == 0) {
     uint32_t before = 0;
     sh.n_miss_total = static_cast<int>(sum_over_cluster(&sh.pub_nmiss, rank, &before));
     sh.miss_off = static_cast<int>(before);
+  } else if (tid == 32) {
     sh.nu_total = static_cast<int>(sum_over_cluster(&sh.pub_nu, rank, nullptr));
-  }
-  if (tid < M) {
+  } else if (tid >= 64 && tid < 64 + M) {
     uint32_t before = 0;
-    sh.nmw[tid] = static_cast<int>(sum_over_cluster(&sh.pub_miss[tid], rank, &before));
-    sh.wmiss_off[tid] = static_cast<int>(before);
-    sh.hits_total[tid] = static_cast<int>(sum_over_cluster(&sh.pub_hit[tid], rank, &before));
-    sh.hit_off[tid] = static_cast<int>(before);
+    sh.nmw[tid - 64] = static_cast<int>(sum_over_cluster(&sh.pub_miss[tid - 64], rank, &before));
+    sh.wmiss_off[tid - 64] = static_cast<int>(before);
+  } else if (tid >= 96 && tid < 96 + M) {
+    uint32_t before = 0;
+    sh.hits_total[tid - 96] = static_cast<int>(sum_over_cluster(&sh.pub_hit[tid - 96], rank, &before));
+    sh.hit_off[tid - 96] = static_cast<int>(before);
   }
   // LRU positions of this CTA in the current order list
   const int step_b = step0;
@@ -973,11 +1113,28 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
                 static_cast<unsigned long long>(n_miss_total));
       atomicAdd(reinterpret_cast<unsigned long long*>(&a.stats[5]),
                 static_cast<unsigned long long>(n_miss_total) * kRowBytes);
+      if (guided) {
+        int nf = 0;
+        for (int m = 0; m < M; ++m) nf += sh.fine[m];
+        atomicAdd(reinterpret_cast<unsigned long long*>(&a.stats[6]), 1ull);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&a.stats[7]),
+                  static_cast<unsigned long long>(nf));
+      }
     }
   }
   // every CTA read the histogram before [S3]: clear it for the next step
   if (rank == 0)
     for (int i = tid; i < M * kHistBins; i += NT) gh[i] = 0u;
+  if (rank == 0 && a.guess != nullptr) {
+    // the same for the fine histogram; every CTA read its guesses at the
+    // start: the next step's indexer flags from one bin below this cut
+    uint32_t* fh = a.fhist + static_cast<size_t>(b) * M * kFineBins;
+    for (int i = tid; i < M * kFineBins; i += NT) fh[i] = 0u;
+    if (tid < M) {
+      const int b1 = sh.b1[tid];
+      a.guess[b * M + tid] = (have_b1 && b1 >= 2) ? static_cast<uint32_t>(b1 - 1) : 0u;
+    }
+  }
 }
 
 // (a4) the rest of the LRU update, after the lists are out: each miss's
@@ -1454,6 +1611,10 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
   a.scores = scores;
   a.ghist = p.scr.ghist;
   a.hist_given = hist_given ? 1 : 0;
+  a.guess = hist_given ? L.guess : nullptr;
+  a.fhist = p.scr.fhist;
+  a.tflag = hist_given ? p.scr.tflag : nullptr;
+  a.nwords = p.scr.nwords;
   a.cache_slots = L.cache_slots;
   a.slot_token = L.slot_token;
   a.last_used = L.last_used;

@@ -64,7 +64,8 @@ class ess_config(ctypes.Structure):
 class ess_stats(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_int64), ("hits", ctypes.c_int64), ("misses", ctypes.c_int64),
                 ("union_size", ctypes.c_int64), ("miss_rows", ctypes.c_int64),
-                ("miss_bytes", ctypes.c_int64)]
+                ("miss_bytes", ctypes.c_int64), ("guided", ctypes.c_int64),
+                ("fine_cuts", ctypes.c_int64)]
 
 
 class EssError(RuntimeError):

@@ -106,6 +106,11 @@ typedef struct {
   int64_t union_size;   /* |U|: distinct rows selected by any way          */
   int64_t miss_rows;    /* |Miss|: distinct rows moved from host           */
   int64_t miss_bytes;   /* miss_rows * D * 2                               */
+  int64_t guided;       /* steps (per request) whose top-k read only the
+                         * tokens the indexer flagged at or above the
+                         * previous step's cut less one bin               */
+  int64_t fine_cuts;    /* ways of those steps whose cut came from the
+                         * indexer's fine histogram (8 more key bits)     */
 } ess_stats;
 
 /* Human-readable name of a status code (static storage). */

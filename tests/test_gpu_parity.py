@@ -303,6 +303,52 @@ def test_stats_counters():
     p.close()
 
 
+def _cut_bins(scores, k):
+    """Coarse bin (top 12 bits of the ordered key) of the k-th largest score."""
+    u = np.ascontiguousarray(scores, dtype=np.float32).view(np.uint32)
+    key = np.where(u >> 31 != 0, ~u, u | np.uint32(0x80000000)).astype(np.uint32)
+    return int(np.sort(key >> 20)[::-1][k - 1])
+
+
+def test_guided_selection_regimes():
+    """From its second step a layer's selection reads only the tokens that the
+    indexer flagged at or above the previous step's cut less one bin, when
+    every way's cut stays at or above that bin; a way whose cut lies in one of
+    the four bins the indexer's fine histogram covers takes it from there.
+    Doubled and halved head weights move every cut by eight bins (an octave):
+    up out of the fine window, then down below the flagged bin (the full
+    scan).  Lists, state and attention follow the oracle bit for bit at every
+    step, and the layer's counters show which of the three ways each request
+    took, as the oracle's own scores predict it."""
+    cfg = W.v32_32k().replace(batch=3, T=8192, T_per_req=[8192, 5000, 300], k=512, C=2048,
+                              mtp=2, mla_heads=32)
+    p = Pair(cfg)
+    base = p.next_inputs
+    guess = np.zeros((cfg.batch, cfg.mtp), dtype=np.int64)
+    seen = set()
+    for f in [1.0, 1.0, 2.0, 2.0, 0.5, 0.5, 0.5]:
+        def scaled(layer, f=f):
+            q, enc, w, qm = base(layer)
+            return q, enc, (w * np.float32(f)).astype(np.float32), qm
+        p.next_inputs = scaled
+        r = p.run_step(check_scores=True)
+        want_guided = want_fine = 0
+        for b in range(cfg.batch):
+            if cfg.k >= int(p.lds[0].T[b]):
+                guess[b] = 0                   # every token selected: no cut
+                continue
+            b1 = [_cut_bins(r.scores[b][m], cfg.k) for m in range(cfg.mtp)]
+            if all(guess[b, m] != 0 and b1[m] >= guess[b, m] for m in range(cfg.mtp)):
+                want_guided += 1
+                want_fine += sum(b1[m] - guess[b, m] < 4 for m in range(cfg.mtp))
+            guess[b] = [x - 1 for x in b1]
+        st = ess.ess_pool_read_stats(p.sess.pool, 0, reset=True)
+        assert (st.guided, st.fine_cuts) == (want_guided, want_fine), f
+        seen.add((want_guided > 0, want_fine > 0))
+    assert seen == {(False, False), (True, False), (True, True)}
+    p.close()
+
+
 def test_device_bounds_check_reports_instead_of_faulting():
     cfg = W.tiny().replace(T=1024, k=128, C=256)
     p = Pair(cfg)
