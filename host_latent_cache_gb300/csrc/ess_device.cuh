@@ -311,6 +311,27 @@ __device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
+__device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// The two halves of a cluster barrier: work placed between them overlaps the
+// wait for the other CTAs (each thread arrives once before it waits).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Bitwise OR into a word of another CTA's shared memory (no return value;
+// ordered before the next cluster barrier's release).
+__device__ __forceinline__ void red_or_dsmem(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.or.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 
 // ---------------------------------------------------------------- compact rows
 // A compact latent row ("ESS: Latent-Cache Offload", the ~656-byte host

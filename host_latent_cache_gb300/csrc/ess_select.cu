@@ -33,7 +33,10 @@
 // entries in list order are exactly the eviction order, so the first
 // |Miss| of them are the victims, already in the order that pairs the i-th
 // miss with the i-th victim; the next list is the remaining unstamped
-// entries followed by the stamped slots in slot order.
+// entries followed by the stamped slots in slot order.  The stamps of the
+// step are also set in a bitmap over the slots, kept in distributed shared
+// memory (CTA r holds the words of its slot range and every CTA ORs its
+// hits into them), which each CTA copies whole to look its list entries up.
 //
 // Two kernels share this work: select_kernel produces everything the step
 // reads (the emitted lists, the miss union and its victims), and
@@ -123,6 +126,7 @@ struct SelShared {
   int n_miss_total, nu_total, miss_off, hit_off[kMaxWays], wmiss_off[kMaxWays], nmw[kMaxWays];
   int hits_total[kMaxWays];
   int unst_before, unst_total;
+  int ndefer;                         // misses whose slot waits for the victims
   int step_b;
   unsigned long long bar;
 };
@@ -321,7 +325,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   extern __shared__ __align__(16) uint8_t dsm[];
   __shared__ SelShared sh;
   pdl_wait_previous();
-  pdl_launch_dependents();
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
@@ -339,9 +342,12 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   int* cslot = lslot + a.lcap;                                        // [c_local] this CTA's LRU list slice
   uint32_t* ckey = reinterpret_cast<uint32_t*>(cslot + a.c_local);    // [M][lcap] candidate keys
   uint32_t* gkey = ckey + M * a.lcap;                                 // [gcap] gathered keys
-  uint8_t* grank = reinterpret_cast<uint8_t*>(gkey + a.gcap);         // [gcap] source rank
+  const int segw = a.c_local / 32;                                    // bitmap words per slot range
+  uint32_t* hseg = gkey + a.gcap;        // [segw] stamps of this CTA's slot range (ORed remotely)
+  uint32_t* hall = hseg + segw;          // [CL * segw] all stamps, copied after [S3]
+  uint32_t* umask = hall + CL * segw;    // [segw] unstamped entries of this CTA's list positions
+  uint8_t* grank = reinterpret_cast<uint8_t*>(umask + segw);          // [gcap] source rank
   uint8_t* lflag = grank + a.gcap;                                    // [lcap] way bits
-  uint8_t* cflag = lflag + a.lcap;                                    // [c_local]
   const int n_local = a.n_local, lcap = a.lcap, Tmax = a.T;
   const bool resident = a.resident != 0;
   const size_t bT = static_cast<size_t>(b) * a.T;
@@ -355,6 +361,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     sh.nl = 0;
     sh.fallback = 0;
     sh.pub_overflow = sh.pub_nmiss = sh.pub_nu = sh.pub_unst = 0;
+    sh.ndefer = 0;
     for (int m = 0; m < kMaxWays; ++m) {
       sh.pub_hit[m] = sh.pub_miss[m] = 0;
       sh.active[m] = 0;
@@ -364,6 +371,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     mbar_init(smem_u32(&sh.bar), 1);
     fence_mbar_init();
   }
+  // the stamp words of this CTA's slots; remote ORs into them come only after
+  // a cluster barrier that every CTA reaches after this
+  for (int i = tid; i < segw; i += NT) hseg[i] = 0u;
   __syncthreads();
 
   // this CTA's positions of the current LRU list (read after the hits are stamped)
@@ -374,6 +384,33 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   cl = cl < 0 ? 0 : (cl > a.c_local ? a.c_local : cl);
   const int32_t* ocur = a.order + (static_cast<size_t>(step0 & 1) * a.B + b) * a.C;
   int32_t* onxt = a.order + (static_cast<size_t>((step0 & 1) ^ 1) * a.B + b) * a.C;
+
+  const bool sel_all = keff >= Tb;  // every token is selected (includes T_b = 0)
+  // the indexer's histogram is final once the previous grid is: this
+  // thread's bins (4095 - 8t - j, j = 0..7, per way) are read while the
+  // scores are still landing
+  const bool pre_hist = !sel_all && a.hist_given;
+  uint32_t c8p[M][8];
+#pragma unroll
+  for (int m = 0; m < M; ++m)
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      c8p[m][j] = pre_hist ? gh[m * kHistBins + kHistBins - 1 - 8 * tid - j] : 0u;
+  // so are the indexer's flag words (this thread's first word of the CTA's
+  // range, the ways OR-ed) and its fine histogram (2M words per thread)
+  const bool pre_guide = pre_hist && a.tflag != nullptr;
+  const int fw0 = r0 >> 5, fw1 = (r0 + nloc + 31) >> 5;
+  uint32_t tw_pre = 0u;
+  if (pre_guide && nloc > 0 && fw0 + tid < fw1)
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+      tw_pre |= a.tflag[(static_cast<size_t>(b) * M + m) * a.nwords + fw0 + tid];
+  static_assert(kFineBins % NT == 0, "fine bins spread evenly over the threads");
+  constexpr int FPT = M * kFineBins / NT;
+  uint32_t fpre[FPT];
+#pragma unroll
+  for (int j = 0; j < FPT; ++j)
+    fpre[j] = pre_guide ? a.fhist[static_cast<size_t>(b) * M * kFineBins + tid + j * NT] : 0u;
 
   // ---------------------------------------------------------------- scores
   {
@@ -396,6 +433,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       for (int i = tid; i < cl; i += NT) cslot[i] = ocur[p0 + i];
     if ((load_scores || bulk_order) && !mbar_wait(smem_u32(&sh.bar), 0, nullptr))
       set_status(a.status, ESS_ERR_TIMEOUT);
+    // the fine bins go to shared memory, free until the candidate passes
+    if (pre_guide)
+#pragma unroll
+      for (int j = 0; j < FPT; ++j) (&sh.hist[0][0])[tid + j * NT] = fpre[j];
     __syncthreads();
   }
   const float* gscores = a.scores + static_cast<size_t>(b) * M * Tmax + r0;
@@ -405,7 +446,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   };
 
   // ---------------------------------------------------------------- (a2) top-k
-  const bool sel_all = keff >= Tb;  // every token is selected (includes T_b = 0)
   if (!sel_all && !a.hist_given) {
     // caller scores: build the 12-bit histogram of this request
     for (int m = 0; m < M; ++m)
@@ -418,13 +458,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     cluster_sync();
   }
   if (!sel_all) {
+#pragma unroll
     for (int m = 0; m < M; ++m) {
       // thread t owns bins 4095 - 8t - j, j = 0..7 (descending order)
       int c8[8];
       int s8 = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        c8[j] = static_cast<int>(gh[m * kHistBins + kHistBins - 1 - 8 * tid - j]);
+        c8[j] = static_cast<int>(pre_hist ? c8p[m][j]
+                                          : gh[m * kHistBins + kHistBins - 1 - 8 * tid - j]);
         s8 += c8[j];
       }
       int tot;
@@ -469,7 +511,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       const uint32_t d = static_cast<uint32_t>(sh.b1[m]) - sh.g[m];
       int fine = 0;
       if (d < static_cast<uint32_t>(kFineWin)) {
-        const uint32_t* F = a.fhist + (static_cast<size_t>(b) * M + m) * kFineBins + d * kFineSub;
+        const uint32_t* F = &sh.hist[0][0] + m * kFineBins + d * kFineSub;
         // lane l owns fine bins 255 - 8l - j, j = 0..7 (descending)
         int c8[8];
         int s8 = 0;
@@ -521,6 +563,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     }
     if (tid == 0) sh.nl = nloc;
     __syncthreads();
+    cluster_sync();   // every CTA's stamp words are zero (the other paths pass one too)
   }
   if (fast) {
     // one ordered pass over this CTA's tokens, each warp over its own
@@ -566,10 +609,12 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         const int w = wb + tid;
         uint32_t bits = 0u;
         if (w < w1 && nloc > 0) {
+          if (wb == w0) {
+            bits = tw_pre;
+          } else {
 #pragma unroll
-          for (int m = 0; m < kMaxWays; ++m) {
-            if (m >= M) break;
-            bits |= a.tflag[(static_cast<size_t>(b) * M + m) * a.nwords + w];
+            for (int m = 0; m < M; ++m)
+              bits |= a.tflag[(static_cast<size_t>(b) * M + m) * a.nwords + w];
           }
           const int tlo = w * 32, thi = r0 + nloc;
           if (tlo < r0) bits &= 0xFFFFFFFFu << (r0 - tlo);
@@ -917,6 +962,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   const int nu = sh.nl;
 
   // ---------------------------------------------------------------- (a3) resolve
+  // The LRU finishing kernel may launch now: its CTAs take their SMs while
+  // this kernel finishes, and only wait for it.  Launched at this kernel's
+  // start instead, they slowed its first phases by a few microseconds.
+  pdl_launch_dependents();
+  // a miss among this thread's first entries: its page-table entry is read
+  // now and used for the prefetch of its host row after [S3]
+  int pf_page = -1;
   for (int e = tid; e < nu; e += NT) {
     const int t = ltok[e];
     int s = a.cache_slots[bT + t];
@@ -925,15 +977,32 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       s = -1;
     }
     lslot[e] = s;
-    if (s >= 0) a.last_used[bC + s] = sh.step_b;   // hits are stamped first
+    if (s >= 0) {
+      a.last_used[bC + s] = sh.step_b;   // hits are stamped first
+      if (lru) {
+        const int ow = s / a.c_local, o = s - ow * a.c_local;
+        red_or_dsmem(dsmem_addr(smem_u32(hseg + (o >> 5)), static_cast<uint32_t>(ow)),
+                     1u << (o & 31));
+      }
+    }
     const uint32_t mk = lflag[e];
     for (int m = 0; m < M; ++m)
       if (mk & (1u << m)) atomicAdd(s >= 0 ? &sh.pub_hit[m] : &sh.pub_miss[m], 1);
     if (s < 0) atomicAdd(&sh.pub_nmiss, 1);
+    if (s < 0 && e == tid && a.host != nullptr && a.page_table != nullptr)
+      pf_page = a.page_table[static_cast<size_t>(b) * (a.T / a.page) + t / a.page];
   }
   if (tid == 0) sh.pub_nu = nu;
   __syncthreads();
   cluster_sync();  // [S3] stamps visible, per-CTA counts published
+  // the whole stamp bitmap, every CTA's words (the remote ORs are complete),
+  // 16 bytes a thread; the first round's reads are in flight with the sums
+  const int nv4 = lru ? CL * segw / 4 : 0;
+  uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+  if (tid < nv4) {
+    const int w = 4 * tid, r = w / segw;
+    hv = ld_dsmem_v4(dsmem_addr(smem_u32(hseg + (w - r * segw)), static_cast<uint32_t>(r)));
+  }
   // the cluster sums, each in a warp of its own so that their remote reads overlap
   if (tid == 0) {
     uint32_t before = 0;
@@ -951,43 +1020,43 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     sh.hit_off[tid - 96] = static_cast<int>(before);
   }
   // LRU positions of this CTA in the current order list
-  const int step_b = step0;
   const int per_wc = (((cl + NW - 1) / NW) + 31) & ~31;
   const int clo = warp * per_wc;
   const int chi = clo + per_wc < cl ? clo + per_wc : cl;
+  if (tid < nv4) *reinterpret_cast<uint4*>(hall + 4 * tid) = hv;
+  for (int q = tid + NT; q < nv4; q += NT) {
+    const int w = 4 * q, r = w / segw;
+    *reinterpret_cast<uint4*>(hall + w) =
+        ld_dsmem_v4(dsmem_addr(smem_u32(hseg + (w - r * segw)), static_cast<uint32_t>(r)));
+  }
+  __syncthreads();
+  int wpre = 0;   // unstamped entries of the warps before this one
   {
-    // unstamped entries among my positions of the list (hits were stamped)
-    int cnt = 0;
-    constexpr int U = 8;   // loads in flight per thread
-    for (int i0 = tid; i0 < cl; i0 += NT * U) {
-      int sv[U], lu[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * NT;
-        int sl = i < cl ? cslot[i] : 0;
+    // unstamped entries among my positions of the list, 32 at a time: their
+    // mask is kept for the placement after [S4]
+    int wcnt = 0;
+    for (int base = clo; base < chi; base += 32) {
+      const int i = base + lane;
+      bool un = false;
+      if (i < chi) {
+        int sl = cslot[i];
         if (sl < 0 || sl >= a.C) {
           set_status(a.status, ESS_ERR_DEVICE_CHECK);
           sl = 0;
+          cslot[i] = 0;
         }
-        sv[u] = sl;
+        un = ((hall[sl >> 5] >> (sl & 31)) & 1u) == 0u;
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) lu[u] = (i0 + u * NT < cl) ? a.last_used[bC + sv[u]] : step_b;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * NT;
-        if (i < cl) {
-          const bool un = lu[u] != step_b;
-          cslot[i] = sv[u];
-          cflag[i] = un ? 1 : 0;
-          cnt += un ? 1 : 0;
-        }
-      }
+      const unsigned bal = __ballot_sync(0xffffffffu, un);
+      if (lane == 0) umask[base >> 5] = bal;
+      wcnt += __popc(bal);
     }
-    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if (lane == 0 && cnt) atomicAdd(&sh.pub_unst, cnt);
+    int total;
+    wpre = warp_base(wcnt, total, sh);
+    if (tid == 0) sh.pub_unst = total;
   }
   __syncthreads();
+  cluster_arrive();  // [S4] unstamped counts published (the miss union goes on meanwhile)
   int n_miss_total = sh.n_miss_total;
   if (n_miss_total > a.C || n_miss_total > MK) {  // cannot happen when C >= min(M*k, T)
     if (tid == 0) set_status(a.status, ESS_ERR_CAPACITY);
@@ -1005,10 +1074,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         lslot[e] = -2 - pos;   // a miss: its index in the request's miss union
         a.miss_tok[static_cast<size_t>(b) * MK + pos] = t;
         if (a.host != nullptr && t < a.T0[b]) {
-          const int pr = a.page_table
-                             ? a.page_table[static_cast<size_t>(b) * (a.T / a.page) + t / a.page] *
-                                       a.page + t % a.page
-                             : t;
+          const int pg = !a.page_table ? 0
+                         : base == 0   ? pf_page
+                                       : a.page_table[static_cast<size_t>(b) * (a.T / a.page) +
+                                                      t / a.page];
+          const int pr = a.page_table ? pg * a.page + t % a.page : t;
           if (pr >= 0 && pr < a.T)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(
                 a.host + (static_cast<size_t>(b) * a.T + pr) * a.row_bytes));
@@ -1016,8 +1086,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       }
     }
   }
-  __syncthreads();
-  cluster_sync();  // [S4] unstamped counts published, miss list visible
+  cluster_wait();  // [S4]
   if (tid == 0) {
     uint32_t before = 0;
     sh.unst_total = static_cast<int>(sum_over_cluster(&sh.pub_unst, rank, &before));
@@ -1028,40 +1097,27 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     // unstamped slots in LRU order: the first |Miss| are the victims, the rest
     // open the next list (each warp places its own contiguous positions);
     // with another policy cl is 0 and victim_kernel lists the victims
-    int wcnt = 0;
+    int pos = sh.unst_before + wpre;
     for (int base = clo; base < chi; base += 32) {
-      const int i = base + lane;
-      wcnt += __popc(__ballot_sync(0xffffffffu, i < chi && cflag[i]));
-    }
-    int total;
-    int pos = sh.unst_before + warp_base(wcnt, total, sh);
-    for (int base = clo; base < chi; base += 32) {
-      const int i = base + lane;
-      const bool f = i < chi && cflag[i];
-      const unsigned bal = __ballot_sync(0xffffffffu, f);
-      if (f) {
-        const int p = pos + __popc(bal & lt);
+      const unsigned msk = umask[base >> 5];
+      if ((msk >> lane) & 1u) {
+        const int p = pos + __popc(msk & lt);
+        const int sl = cslot[base + lane];
         if (p < n_miss_total)
-          a.vlist[static_cast<size_t>(b) * MK + p] = cslot[i];
+          a.vlist[static_cast<size_t>(b) * MK + p] = sl;
         else if (p - n_miss_total < a.C)
-          onxt[p - n_miss_total] = cslot[i];
+          onxt[p - n_miss_total] = sl;
       }
-      pos += __popc(bal);
+      pos += __popc(msk);
     }
   }
-  __syncthreads();
-  cluster_sync();  // [S5] victims listed; no shared memory is read remotely after this
-  if (n_miss_total > 0 && lru) {
-    // the i-th miss goes to the i-th victim (the state rewrite and the rest of
-    // the next LRU list are left to lru_finish_kernel)
-    const int per = (n_miss_total + CL - 1) / CL;
-    const int i0 = static_cast<int>(rank) * per;
-    const int i1 = i0 + per < n_miss_total ? i0 + per : n_miss_total;
-    for (int i = i0 + tid; i < i1; i += NT)
-      a.miss_slot[static_cast<size_t>(b) * MK + i] = a.vlist[static_cast<size_t>(b) * MK + i];
-  }
+  cluster_arrive();  // [S5] victims listed (the lists go out meanwhile)
 
   // ---------------------------------------------------------------- emit per-way lists
+  // Misses first, then hits, each in token order.  Under LRU a miss's slot is
+  // its victim's, listed by whichever CTA holds that position of the LRU list:
+  // it is written after [S5] from a deferred (way, position, miss index).
+  uint32_t* defer = ckey;   // the candidate keys are no longer needed
   for (int m = 0; m < M; ++m) {
     int runm = sh.wmiss_off[m];
     int runh = sh.nmw[m] + sh.hit_off[m];
@@ -1076,15 +1132,20 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         fm = s < 0;
         fh = !fm;
       }
-      const int pm = ordered_pos(fm ? 1 : 0, runm, sh, parity);
-      const int ph = ordered_pos(fh ? 1 : 0, runh, sh, parity);
+      // one scan for both lists: misses in the low half-word, hits in the high
+      int tot;
+      const int ex = block_scan((fm ? 1 : 0) | (fh ? 1 << 16 : 0), tot, sh, parity);
+      const int pm = runm + (ex & 0xFFFF), ph = runh + (ex >> 16);
+      runm += tot & 0xFFFF;
+      runh += tot >> 16;
       if (fm && pm < a.k) {
         const int mi = -2 - s;
         a.topk_idx[wo + pm] = t;
         if (lru) {
-          const int ns =
-              (mi >= 0 && mi < n_miss_total) ? a.vlist[static_cast<size_t>(b) * MK + mi] : 0;
-          a.topk_slot[wo + pm] = ~ns;
+          const int d = atomicAdd(&sh.ndefer, 1);
+          // way (2 bits), position (13 bits: k <= 8192), miss index + 1 (14 bits, 0: none)
+          defer[d] = (static_cast<uint32_t>(m) << 27) | (static_cast<uint32_t>(pm) << 14) |
+                     static_cast<uint32_t>(mi >= 0 && mi < MK ? mi + 1 : 0);
         } else {
           a.topk_slot[wo + pm] = -2 - mi;   // its miss index; victim_kernel puts ~slot here
         }
@@ -1094,6 +1155,24 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         a.topk_slot[wo + ph] = s;
       }
     }
+  }
+  cluster_wait();  // [S5] no shared memory is read remotely after this
+  __syncthreads();
+  if (n_miss_total > 0 && lru) {
+    // the i-th miss goes to the i-th victim (the state rewrite and the rest of
+    // the next LRU list are left to lru_finish_kernel)
+    const int per = (n_miss_total + CL - 1) / CL;
+    const int i0 = static_cast<int>(rank) * per;
+    const int i1 = i0 + per < n_miss_total ? i0 + per : n_miss_total;
+    for (int i = i0 + tid; i < i1; i += NT)
+      a.miss_slot[static_cast<size_t>(b) * MK + i] = a.vlist[static_cast<size_t>(b) * MK + i];
+  }
+  for (int i = tid; i < sh.ndefer; i += NT) {
+    const uint32_t d = defer[i];
+    const int m = static_cast<int>(d >> 27), pm = static_cast<int>((d >> 14) & 0x1FFF);
+    const int mi = static_cast<int>(d & 0x3FFF) - 1;
+    const int ns = (mi >= 0 && mi < n_miss_total) ? a.vlist[static_cast<size_t>(b) * MK + mi] : 0;
+    a.topk_slot[(static_cast<size_t>(b) * M + m) * a.k + pm] = ~ns;
   }
   if (rank == 0 && tid == 0) {
     for (int m = 0; m < M; ++m) a.n_miss_way[b * M + m] = sh.nmw[m];
@@ -1581,14 +1660,19 @@ SelSizes sel_sizes(const ess_config& c, int T_hmax) {
   z.nl = (T_hmax + CL - 1) / CL;
   z.nl = ((z.nl + 3) / 4) * 4;
   if (z.nl < 4) z.nl = 4;
-  z.c_local = (c.C + CL - 1) / CL;
+  // slots per CTA: a multiple of 128, so that each CTA's range of the stamp
+  // bitmap is whole 16-byte units of words
+  z.c_local = ((c.C + CL - 1) / CL + 127) / 128 * 128;
   const int MK = c.mtp * c.k;
   z.lcap = z.nl < MK ? z.nl : MK;   // the union of one CTA's tokens never exceeds this
   z.lcap = (z.lcap + 3) / 4 * 4;    // keeps the arrays after the list 16-byte aligned
   z.gcap = 4096;
   z.res_bytes = static_cast<size_t>(c.mtp) * z.nl * 4;
-  z.fixed = static_cast<size_t>(z.lcap) * (9 + 4 * c.mtp) + static_cast<size_t>(z.c_local) * 5 +
-            static_cast<size_t>(z.gcap) * 5 + 64;
+  // lists, the LRU slice, candidate keys, gathered keys and ranks, and the
+  // stamp bitmap words (own range, all ranges, unstamped masks)
+  z.fixed = static_cast<size_t>(z.lcap) * (9 + 4 * c.mtp) + static_cast<size_t>(z.c_local) * 4 +
+            static_cast<size_t>(z.gcap) * 5 + static_cast<size_t>(z.c_local / 32) * (CL + 2) * 4 +
+            64;
   return z;
 }
 
