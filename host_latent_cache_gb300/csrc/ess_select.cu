@@ -118,7 +118,7 @@ struct SelShared {
   int fallback;
   int nl;
   int ncand[kMaxWays];                // this CTA's candidates per way (read through DSMEM)
-  int gcnt[CL];                       // every CTA's candidate count for the way being gathered
+  int gcnt[kMaxWays][CL];             // every CTA's candidate count per way (read once)
   int gsel;                           // 1: candidates are gathered into every CTA
   // published for the other CTAs of the cluster (read through DSMEM)
   int pub_overflow, pub_nmiss, pub_nu, pub_hit[kMaxWays], pub_miss[kMaxWays], pub_unst;
@@ -556,6 +556,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     }
     __syncthreads();
   }
+  // cache slots of the listed tokens, read as soon as the list is out and
+  // carried through the filter (its first four rounds), so that the resolve
+  // reads them from shared memory
+  int csr[4] = {-1, -1, -1, -1};
+  bool cs_ready = false;
   if (sel_all) {
     for (int i = tid; i < nloc; i += NT) {
       ltok[i] = r0 + i;
@@ -729,10 +734,29 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     }
     __syncthreads();
     cluster_sync();  // lists and candidate keys complete; overflow flags published
-    if (tid == 0)
-      sh.fallback = sum_over_cluster(&sh.pub_overflow, 0, nullptr) ? 1 : 0;
+    // every CTA's overflow flag and candidate counts, in one round of remote reads
+    if (tid < CL) {
+      const uint32_t r = static_cast<uint32_t>(tid);
+      const uint32_t ovf = ld_dsmem_u32(dsmem_addr(smem_u32(&sh.pub_overflow), r));
+      uint32_t nc[M];
+#pragma unroll
+      for (int m = 0; m < M; ++m) nc[m] = ld_dsmem_u32(dsmem_addr(smem_u32(&sh.ncand[m]), r));
+#pragma unroll
+      for (int m = 0; m < M; ++m) sh.gcnt[m][tid] = static_cast<int>(nc[m]);
+      if (ovf) sh.fallback = 1;
+    }
     __syncthreads();
     fast = !sh.fallback;
+    // (read after the list barrier: loads still in flight at a cluster
+    // barrier's release would hold it up)
+    if (fast) {
+      const int nl = sh.nl;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {   // the filter's entry-to-thread mapping
+        const int e = q * NT + tid;
+        csr[q] = e < nl ? a.cache_slots[bT + ltok[e]] : -1;
+      }
+    }
   }
   if (fast) {
     const int nl = sh.nl;
@@ -743,15 +767,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       // exact threshold locally: the same result in every CTA, no more barriers
       for (int m = 0; m < M; ++m) {
         if (!sh.active[m]) continue;
-        // every CTA's count first, then all the remote reads at once
-        if (tid < CL)
-          sh.gcnt[tid] = static_cast<int>(
-              ld_dsmem_u32(dsmem_addr(smem_u32(&sh.ncand[m]), static_cast<uint32_t>(tid))));
-        __syncthreads();
+        // every CTA's count (read with the overflow flags), then all the remote reads at once
         int roff[CL + 1];
         roff[0] = 0;
 #pragma unroll
-        for (int r = 0; r < CL; ++r) roff[r + 1] = roff[r] + sh.gcnt[r];
+        for (int r = 0; r < CL; ++r) roff[r + 1] = roff[r] + sh.gcnt[m][r];
         const int off = roff[CL];
         const int ngc = off < a.gcap ? off : a.gcap;
         const int need0 = sh.remaining[m];   // unchanged until after the next barrier
@@ -868,6 +888,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
         tok = ltok[e];
         f = lflag[e];
       }
+      int cs = -1;
+      if (base < 4 * NT) {
+        cs = csr[0];
+        csr[0] = csr[1];
+        csr[1] = csr[2];
+        csr[2] = csr[3];
+      } else if (e < nl) {
+        cs = a.cache_slots[bT + tok];
+      }
       uint32_t sel = f & 0xFu;
 #pragma unroll
       for (int m = 0; m < kMaxWays; ++m) {
@@ -889,8 +918,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       if (sel) {
         ltok[pos] = tok;
         lflag[pos] = static_cast<uint8_t>(sel);
+        lslot[pos] = cs;
       }
     }
+    cs_ready = true;
     if (tid == 0) sh.nl = nu;
     __syncthreads();
   } else if (!sel_all) {
@@ -971,7 +1002,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   int pf_page = -1;
   for (int e = tid; e < nu; e += NT) {
     const int t = ltok[e];
-    int s = a.cache_slots[bT + t];
+    int s = cs_ready ? lslot[e] : a.cache_slots[bT + t];
     if (s >= a.C || s < -1) {
       set_status(a.status, ESS_ERR_DEVICE_CHECK);
       s = -1;
