@@ -152,6 +152,10 @@ constexpr int kInPerThread = 2;
 
 __global__ void __launch_bounds__(256) inputs_in_kernel(const InSeg s0, const InSeg s1,
                                                         const InSeg s2) {
+  // The indexer after this kernel may launch at once: it loads its first key
+  // tiles beside the previous step's last kernel, as it does without this one,
+  // and waits for this grid (and so for that kernel) before it reads a query.
+  pdl_launch_dependents();
   const long long i0 =
       (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * kInPerThread;
   uint4 v[kInPerThread];
@@ -172,7 +176,6 @@ __global__ void __launch_bounds__(256) inputs_in_kernel(const InSeg s0, const In
     }
   }
   pdl_wait_previous();
-  pdl_launch_dependents();
 #pragma unroll
   for (int u = 0; u < kInPerThread; ++u)
     if (d[u]) *d[u] = v[u];
