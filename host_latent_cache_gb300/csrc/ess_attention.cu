@@ -37,8 +37,8 @@ constexpr uint32_t kBlk = 16384;         // one [128 rows x 64 dims] bf16 block
 constexpr int kDimBlocks = kRowDim / 64; // 9
 constexpr uint32_t kRowsBytes = kDimBlocks * kBlk;   // 147456
 constexpr uint32_t kQBytes = QST * kBlk;             // 65536
-constexpr int kMergeBatch = 4;       // chunk partials in flight per merge thread
-constexpr int kMergeMinBlocks = 12;  // merge CTAs per SM the register budget allows
+constexpr int kMergeBatch = 8;       // chunk partials in flight per merge thread
+constexpr int kMergeMinBlocks = 8;   // merge CTAs per SM the register budget allows
 
 struct AttnArgs {
   const int32_t* topk_idx;    // [B][M][k]
@@ -395,9 +395,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // kMergeBatch chunks at a time, rescaling the running sums when M grows).  One
 // CTA per (head, request-way); thread t owns dims 4t..4t+3.  Launched as a
 // programmatic dependent of the attention kernel: it waits for that grid
-// before reading the partials.  Few registers per thread, so that every CTA
-// is resident at once beside the attention CTAs (a second wave would add its
-// whole latency to the step).
+// before reading the partials.  Eight chunks' loads are in flight per thread
+// (two rounds of L2 latency instead of four), with few enough registers that
+// every CTA is still resident beside the attention CTAs (a second wave would
+// add its whole latency to the step).
 __global__ void __launch_bounds__(128, kMergeMinBlocks) merge_kernel(const uint16_t* __restrict__ part_o,
                                                     const float2* __restrict__ part_ml,
                                                     float* __restrict__ out, int H, int nch) {

@@ -1009,7 +1009,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     }
     lslot[e] = s;
     if (s >= 0) {
-      a.last_used[bC + s] = sh.step_b;   // hits are stamped first
+      // the hit's stamp in last_used is written after the last cluster barrier
+      // (nothing in this kernel reads it; a store still in flight would hold a
+      // barrier's release); the stamp bitmap carries it to the LRU scan
       if (lru) {
         const int ow = s / a.c_local, o = s - ow * a.c_local;
         red_or_dsmem(dsmem_addr(smem_u32(hseg + (o >> 5)), static_cast<uint32_t>(ow)),
@@ -1124,25 +1126,39 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     sh.unst_before = static_cast<int>(before);
   }
   __syncthreads();
-  {
-    // unstamped slots in LRU order: the first |Miss| are the victims, the rest
-    // open the next list (each warp places its own contiguous positions);
-    // with another policy cl is 0 and victim_kernel lists the victims
-    int pos = sh.unst_before + wpre;
-    for (int base = clo; base < chi; base += 32) {
+  // Unstamped slots in LRU order: the first |Miss| are the victims, the rest
+  // open the next list (each warp places its own contiguous positions); with
+  // another policy cl is 0 and victim_kernel lists the victims.  The victims,
+  // which other CTAs read, go out before the barrier; the next list after it.
+  const int upos0 = sh.unst_before + wpre;
+  if (sh.unst_before < n_miss_total) {
+    int pos = upos0;
+    for (int base = clo; base < chi && pos < n_miss_total; base += 32) {
       const unsigned msk = umask[base >> 5];
       if ((msk >> lane) & 1u) {
         const int p = pos + __popc(msk & lt);
-        const int sl = cslot[base + lane];
-        if (p < n_miss_total)
-          a.vlist[static_cast<size_t>(b) * MK + p] = sl;
-        else if (p - n_miss_total < a.C)
-          onxt[p - n_miss_total] = sl;
+        if (p < n_miss_total) a.vlist[static_cast<size_t>(b) * MK + p] = cslot[base + lane];
       }
       pos += __popc(msk);
     }
   }
   cluster_arrive();  // [S5] victims listed (the lists go out meanwhile)
+  {
+    int pos = upos0;
+    for (int base = clo; base < chi; base += 32) {
+      const unsigned msk = umask[base >> 5];
+      if ((msk >> lane) & 1u) {
+        const int p = pos + __popc(msk & lt) - n_miss_total;
+        if (p >= 0 && p < a.C) onxt[p] = cslot[base + lane];
+      }
+      pos += __popc(msk);
+    }
+    // the hits' stamps (misses' slots are stamped by lru_finish_kernel)
+    for (int e = tid; e < nu; e += NT) {
+      const int s = lslot[e];
+      if (s >= 0) a.last_used[bC + s] = sh.step_b;
+    }
+  }
 
   // ---------------------------------------------------------------- emit per-way lists
   // Misses first, then hits, each in token order.  Under LRU a miss's slot is
