@@ -413,11 +413,19 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     fpre[j] = pre_guide ? a.fhist[static_cast<size_t>(b) * M * kFineBins + tid + j * NT] : 0u;
 
   // ---------------------------------------------------------------- scores
+  // The scores (and the order slice) land in shared memory by bulk copy; the
+  // wait for them comes before the first code that reads them there, so the
+  // bin search and the guided listing (which reads its few scores from global
+  // memory) run while they land.
+  const bool load_scores = resident && nloc > 0;
+  // the order list slice is copied in 16-byte units when aligned, else by threads
+  const bool bulk_order = cl > 0 && (cl & 3) == 0 && (p0 & 3) == 0 && (a.C & 3) == 0;
+  auto wait_bulk = [&]() {   // idempotent: phase 0 stays complete
+    if ((load_scores || bulk_order) && !mbar_wait(smem_u32(&sh.bar), 0, nullptr))
+      set_status(a.status, ESS_ERR_TIMEOUT);
+  };
   {
     const int cnt = ((nloc + 3) / 4) * 4 <= Tmax - r0 ? ((nloc + 3) / 4) * 4 : Tmax - r0;
-    const bool load_scores = resident && nloc > 0;
-    // the order list slice is copied in 16-byte units when aligned, else by threads
-    const bool bulk_order = cl > 0 && (cl & 3) == 0 && (p0 & 3) == 0 && (a.C & 3) == 0;
     if (tid == 0 && (load_scores || bulk_order)) {
       uint32_t bytes = (load_scores ? cnt * 4 * M : 0) + (bulk_order ? cl * 4 : 0);
       mbar_arrive_expect_tx(smem_u32(&sh.bar), bytes);
@@ -431,8 +439,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     }
     if (!bulk_order)
       for (int i = tid; i < cl; i += NT) cslot[i] = ocur[p0 + i];
-    if ((load_scores || bulk_order) && !mbar_wait(smem_u32(&sh.bar), 0, nullptr))
-      set_status(a.status, ESS_ERR_TIMEOUT);
     // the fine bins go to shared memory, free until the candidate passes
     if (pre_guide)
 #pragma unroll
@@ -447,6 +453,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
 
   // ---------------------------------------------------------------- (a2) top-k
   if (!sel_all && !a.hist_given) {
+    wait_bulk();
     // caller scores: build the 12-bit histogram of this request
     for (int m = 0; m < M; ++m)
       for (int base = 0; base < nloc; base += NT) {
@@ -567,6 +574,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       lflag[i] = static_cast<uint8_t>((1u << M) - 1u);
     }
     if (tid == 0) sh.nl = nloc;
+    wait_bulk();
     __syncthreads();
     cluster_sync();   // every CTA's stamp words are zero (the other paths pass one too)
   }
@@ -603,11 +611,30 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
       }
       return f;
     };
+    // the flags of one token from its scores (M ways)
+    auto flags_of = [=](const float* sv) -> uint32_t {
+      uint32_t f = 0;
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const uint32_t key = float_key(sv[m] + 0.0f);
+        if (key >= hi_k[m]) f |= 1u << m;
+        else if (key >= lo_k[m]) f |= 16u << m;
+      }
+      return f;
+    };
+    auto flags_global = [=](int i) -> uint32_t {
+      float sv[M];
+#pragma unroll
+      for (int m = 0; m < M; ++m) sv[m] = gscores[static_cast<size_t>(m) * Tmax + i];
+      return flags_of(sv);
+    };
     int total;
     if (guided) {
       // the flagged tokens only: one flag word per thread (the ways' words
-      // OR-ed, clipped to this CTA's tokens); its tokens that the keys place
-      // at or above the cut are counted, given ordered positions, and listed
+      // OR-ed, clipped to this CTA's tokens).  The scores of a word's first
+      // eight flagged tokens are read from global memory together, the rest
+      // one by one; the tokens that the keys place at or above the cut are
+      // counted, given ordered positions, and listed.
       const int w0 = r0 >> 5, w1 = (r0 + nloc + 31) >> 5;
       int run = 0;
       for (int wb = w0; wb < w1; wb += NT) {
@@ -625,23 +652,59 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
           if (tlo < r0) bits &= 0xFFFFFFFFu << (r0 - tlo);
           if (thi - tlo < 32) bits &= (1u << (thi - tlo)) - 1u;
         }
-        uint32_t q = 0u;
-        for (uint32_t x = bits; x != 0u; x &= x - 1u) {
-          const int j = __ffs(x) - 1;
-          if (coarse_flags(w * 32 + j - r0)) q |= 1u << j;
+        constexpr int NB = 8;
+        int jj[NB];
+        uint32_t x = bits;
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+          jj[u] = -1;
+          if (x != 0u) {
+            jj[u] = __ffs(x) - 1;
+            x &= x - 1u;
+          }
         }
-        int p = ordered_pos(__popc(q), run, sh, parity);
-        for (uint32_t x = q; x != 0u; x &= x - 1u) {
-          const int i = w * 32 + (__ffs(x) - 1) - r0;
+        const uint32_t rest = x;   // flagged tokens past the first eight
+        float sv[NB][M];
+#pragma unroll
+        for (int u = 0; u < NB; ++u)
+#pragma unroll
+          for (int m = 0; m < M; ++m)
+            sv[u][m] = jj[u] >= 0 ? gscores[static_cast<size_t>(m) * Tmax + (w * 32 + jj[u] - r0)]
+                                  : 0.0f;
+        uint32_t fl[NB];
+        uint32_t q = 0u;
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+          fl[u] = jj[u] >= 0 ? flags_of(sv[u]) : 0u;
+          q += fl[u] ? 1u : 0u;
+        }
+        for (uint32_t y = rest; y != 0u; y &= y - 1u)
+          q += flags_global(w * 32 + (__ffs(y) - 1) - r0) ? 1u : 0u;
+        int p = ordered_pos(static_cast<int>(q), run, sh, parity);
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+          if (fl[u] == 0u) continue;
+          if (p < lcap) {
+            ltok[p] = w * 32 + jj[u];
+            lflag[p] = static_cast<uint8_t>(fl[u]);
+          }
+          ++p;
+        }
+        for (uint32_t y = rest; y != 0u; y &= y - 1u) {
+          const int i = w * 32 + (__ffs(y) - 1) - r0;
+          const uint32_t f = flags_global(i);
+          if (f == 0u) continue;
           if (p < lcap) {
             ltok[p] = r0 + i;
-            lflag[p] = static_cast<uint8_t>(coarse_flags(i));
+            lflag[p] = static_cast<uint8_t>(f);
           }
           ++p;
         }
       }
       total = run;
+      wait_bulk();   // the candidate keys and the filter read the staged scores
     } else {
+    wait_bulk();
     const int per_w = (((nloc + NW - 1) / NW) + 31) & ~31;
     const int wlo = warp * per_w;
     const int whi = wlo + per_w < nloc ? wlo + per_w : nloc;
@@ -926,6 +989,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     __syncthreads();
   } else if (!sel_all) {
     // fallback: exact radix passes over every token
+    wait_bulk();
     if (tid < M) {
       sh.active[tid] = 1;
       sh.remaining[tid] = keff;
