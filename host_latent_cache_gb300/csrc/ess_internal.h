@@ -33,9 +33,11 @@ constexpr int kFineBins = kFineWin * kFineSub;
 #endif
 constexpr int kIdxMaxStages = ESS_IDX_MAX_STAGES;
 constexpr int kIdxMinStages = 2;
-// tiles per chunk: the indexer's barrier rounds move up to this many 128-token tiles
+// tiles per chunk: the indexer's barrier rounds move up to this many 128-token
+// tiles (three: three 48 KB ring stages fit beside the rest, where four-tile
+// chunks leave room for two 64 KB stages only)
 #ifndef ESS_IDX_SUB
-#define ESS_IDX_SUB 4
+#define ESS_IDX_SUB 3
 #endif
 constexpr int kIdxSubMax = ESS_IDX_SUB;
 constexpr int kIdxTile = 128;         // tokens per tile (MMA M)
