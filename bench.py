@@ -459,7 +459,8 @@ def indexer_source_digest() -> str:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     with open(os.path.join(csrc, INDEXER_CONSTANTS), "rb") as f:
-        h.update(b"".join(l for l in f.read().splitlines(True) if b"constexpr" in l))
+        h.update(b"".join(l for l in f.read().splitlines(True)
+                          if b"constexpr" in l or l.lstrip().startswith(b"#define")))
     return h.hexdigest()[:16]
 
 
