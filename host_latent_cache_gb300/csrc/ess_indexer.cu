@@ -58,7 +58,6 @@ struct IdxArgs {
 
 constexpr uint32_t kTileBytes = kIdxTile * kKeyRowBytes;  // 16 KB
 constexpr int kMaxAcc = 8;   // TMEM accumulators in flight (A * N <= 512 columns)
-constexpr int kScaleRing = 16;   // key-scale ring: one 512-byte entry per tile (>= S + A)
 
 // Walks a CTA's tiles in order over the concatenated requests: request b
 // owns tiles [lo, hi); the tile prefix is read only when the request changes.
@@ -129,8 +128,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   // the fine histograms follow the coarse ones: M x kFineBins
   const int HC = a.ghist ? a.M * kHistBins : 0;
   const int HB = HC + (a.ghist && a.guess ? a.M * kFineBins : 0);
-  float* sring = reinterpret_cast<float*>(hist + HB);   // [kScaleRing][U x 128] key scales
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sring + kScaleRing * U * kIdxTile);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(hist + HB);
   uint64_t* full = bars;
   uint64_t* empty = full + S;
   uint64_t* accf = empty + S;
@@ -139,9 +137,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   uint64_t* qempty = qfull + 2;
   uint64_t* epdone = qempty + 2;      // every epilogue thread has counted its tokens
   uint64_t* fldone = epdone + 2;      // the histogram is flushed and clear again
-  uint64_t* sfull = fldone + 2;       // [kScaleRing] a chunk's key scales have landed
-  uint64_t* sempty = sfull + kScaleRing;   // [kScaleRing] its epilogue group has read them
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + kScaleRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fldone + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* consumed = abort_flag + 1;
 
@@ -169,10 +165,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       mbar_init(smem_u32(&epdone[i]), 256);
       mbar_init(smem_u32(&fldone[i]), 256);
     }
-    for (int i = 0; i < kScaleRing; ++i) {
-      mbar_init(smem_u32(&sfull[i]), 1);
-      mbar_init(smem_u32(&sempty[i]), 128);
-    }
     *abort_flag = 0;
     *consumed = 0;
     fence_mbar_init();
@@ -193,26 +185,17 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // the keys (and key scales) of chunk it: n tiles from tile j0 of request b
-  // into stage it % S; the scales, 4 bytes per token (a multiple of 16 bytes,
-  // since max_T is a multiple of 4), into ring entry it % kScaleRing
+  // the keys of chunk it: n tiles from tile j0 of request b into stage it % S
+  // (the epilogue threads read their tokens' key scales from global memory)
   auto issue_chunk = [&](int it, int b, int j0, int n) {
     const int s = it % S;
     mbar_arrive_expect_tx(smem_u32(&full[s]), static_cast<uint32_t>(n) * kTileBytes);
     for (int u = 0; u < n; ++u)
       tma_load_2d(smem_u32(kst + s * stage_bytes + u * kTileBytes), &kmap, smem_u32(&full[s]), 0,
                   b * a.T + (j0 + u) * kIdxTile);
-    if (a.scale != nullptr) {
-      const int r = it % kScaleRing;
-      const int t0 = j0 * kIdxTile;
-      const int nt = a.T - t0 < n * kIdxTile ? a.T - t0 : n * kIdxTile;
-      mbar_arrive_expect_tx(smem_u32(&sfull[r]), static_cast<uint32_t>(nt * 4));
-      bulk_load(smem_u32(sring + r * U * kIdxTile), a.scale + static_cast<size_t>(b) * a.T + t0,
-                static_cast<uint32_t>(nt * 4), smem_u32(&sfull[r]));
-    }
   };
   // Early mode: no append kernel has run on this layer since its last indexer,
-  // so the tile prefix and the key rows (and scales) of the first chunks are
+  // so the tile prefix and the key rows of the first chunks are
   // final already; the first ring's worth is requested before the wait.
   int n_early = 0;
   if (warp == 0 && a.early) {
@@ -265,9 +248,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       if (lane == 0 && it >= n_early) {
         const int s = it % S;
         if (it >= S) w_ok = mbar_wait(smem_u32(&empty[s]), ((it / S) - 1) & 1, abort_flag) ? 1 : 0;
-        if (w_ok && a.scale != nullptr && it >= kScaleRing)
-          w_ok = mbar_wait(smem_u32(&sempty[it % kScaleRing]), ((it / kScaleRing) - 1) & 1,
-                           abort_flag) ? 1 : 0;
         if (w_ok) issue_chunk(it, b, j0, n);
       }
       w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
@@ -284,9 +264,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       const int issued = it > n_early ? it : n_early;
       for (int i = *consumed; i < issued; ++i)
         mbar_wait(smem_u32(&full[i % S]), (i / S) & 1, nullptr);
-      if (a.scale != nullptr)
-        for (int i = issued > kScaleRing ? issued - kScaleRing : 0; i < issued; ++i)
-          mbar_wait(smem_u32(&sfull[i % kScaleRing]), (i / kScaleRing) & 1, nullptr);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
@@ -420,6 +397,15 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           gm[m] = (HB > HC && m < MW) ? a.guess[b * MW + m] : 0u;
       }
       if ((it & 1) == grp) {
+        // this thread's key scales of the chunk, read while its MMAs run
+        float scv[kIdxSubMax];
+#pragma unroll
+        for (int u = 0; u < kIdxSubMax; ++u) {
+          const int t = (j0 + u) * kIdxTile + row;
+          scv[u] = (u < n && t < Tcur && a.scale != nullptr)
+                       ? __ldg(a.scale + static_cast<size_t>(b) * a.T + t)
+                       : 1.0f;
+        }
         const int acc = it % A;
         ok = mbar_wait(smem_u32(&accf[acc]), (it / A) & 1, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
@@ -435,20 +421,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           if (u < n) head_sums(lane_base + static_cast<uint32_t>((acc * U + u) * NP), wq, smv[u]);
         tc_fence_before();
         mbar_arrive(smem_u32(&acce[acc]));
-        // the tokens' key scales, staged in shared memory with the chunk
-        const int r = it % kScaleRing;
-        if (a.scale != nullptr) {
-          bool any = false;
-          for (int u = 0; u < n; ++u) any |= (j0 + u) * kIdxTile + row < Tcur;
-          if (any) ok = mbar_wait(smem_u32(&sfull[r]), (it / kScaleRing) & 1, abort_flag);
-        }
 #pragma unroll
         for (int u = 0; u < kIdxSubMax; ++u) {
           if (u >= n) continue;   // the same in every lane
           const int t = (j0 + u) * kIdxTile + row;
           const bool valid = t < Tcur;
-          const float sc =
-              (valid && a.scale != nullptr) ? sring[(r * U + u) * kIdxTile + row] : 1.0f;
+          const float sc = scv[u];
           const int word = (j0 + u) * (kIdxTile / 32) + quad;   // this warp's 32 tokens
 #pragma unroll
           for (int m = 0; m < kMaxWays; ++m) {   // unrolled: the sums stay in registers
@@ -471,7 +449,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             }
           }
         }
-        if (a.scale != nullptr) mbar_arrive(smem_u32(&sempty[r]));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
@@ -509,8 +486,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
 
 size_t indexer_smem_bytes(int S, int U, int NP, int HB) {
   return 1024 + static_cast<size_t>(S) * U * kTileBytes + 2u * NP * 128 + 2u * NP * 4 +
-         HB * 4u + static_cast<size_t>(kScaleRing) * U * kIdxTile * 4 +
-         (2 * S + 2 * kMaxAcc + 8 + 2 * kScaleRing) * 8 + 16;
+         HB * 4u + (2 * S + 2 * kMaxAcc + 8) * 8 + 16;
 }
 
 // Tiles per chunk and key-ring stages for a query width: as many tiles per
