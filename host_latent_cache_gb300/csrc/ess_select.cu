@@ -21,12 +21,17 @@
 // Top-k: a histogram of the top 12 bits of the order-preserving score keys
 // (filled by the indexer, or built here for caller scores) gives the bin
 // that holds the k-th largest score.  One ordered pass lists the tokens
-// above that bin (selected) and in it (candidates); MSB radix passes over
-// the candidates' low 20 bits, with per-CTA histograms summed through
-// distributed shared memory, fix the exact threshold; equal keys go to the
-// lowest token.  If the candidates could overflow the list, the kernel
-// falls back to radix passes over every token.  All lists come out in
-// ascending token order.
+// above that bin (selected) and in it (candidates).  When the indexer has
+// flagged the tokens at or above the previous step's cut less one bin and
+// the cut has not fallen below that bin, the pass reads only the flagged
+// tokens, and when the cut's bin is one of the four the indexer's fine
+// histogram covers, the candidates are those of one 4096-wide fine bin.
+// The candidates' keys are gathered through distributed shared memory into
+// every CTA and ranked one against another (up to 128) or by MSB radix
+// passes over their low 20 bits, which fix the exact threshold; equal keys
+// go to the lowest token.  If a CTA's list could overflow, the kernel falls
+// back to radix passes over every token.  Every path gives the same exact
+// result; all lists come out in ascending token order.
 //
 // LRU: the slots are kept in a list sorted by (last_used, slot), double
 // buffered by step parity.  After the hits are stamped, the unstamped
