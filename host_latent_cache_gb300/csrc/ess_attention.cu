@@ -27,6 +27,7 @@
 // programmatic dependent of this one, merges the partials of every (request,
 // way) with the usual log-sum-exp weights.
 #include "ess_device.cuh"
+#include "ess_sync.cuh"
 
 namespace ess {
 namespace {
@@ -56,11 +57,13 @@ struct AttnArgs {
   float c2;                   // sm_scale * log2(e)
   int staged;
   int compact;                // host rows are compact 656-byte rows, widened on the way
-  // 1: the previous kernel on the stream is the LRU finishing kernel, whose
-  // own predecessor (the selection that wrote the lists read here) completed
-  // before this grid could launch; the wait for the finishing kernel moves to
-  // the end so the two run side by side
+  // 1: the previous kernel on the stream is the LRU finishing kernel of the
+  // selection that wrote the lists read here.  The grid may launch while that
+  // selection still runs: each CTA waits for its request's counter in ready
+  // instead, and the wait for the finishing kernel moves to the end so the
+  // two run side by side
   int early;
+  const int* ready;           // [B] completion counters of the selection (early only)
 };
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -123,6 +126,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_arrive_expect_tx(smem_u32(&qfull[s]), kBlk);
       tma_load_2d(smem_u32(qst + s * kBlk), &qmap, smem_u32(&qfull[s]), s * 64, qrow0);
     }
+  }
+  if (a.early) {
+    // request b's lists are out once every selection CTA of it has counted
+    // itself (all of them are resident: they let the finishing kernel, and it
+    // this grid, launch).  Past the limit the chunk is treated as empty.
+    __shared__ int lists_ok;
+    if (tid == 0) {
+      lists_ok = wait_count(a.ready + b, kSelCluster) ? 1 : 0;
+      if (!lists_ok) set_status(a.status, ESS_ERR_TIMEOUT);
+    }
+    __syncthreads();
+    if (!lists_ok) cnt = 0;
   }
 
   // ------------------------------------------------ gather
@@ -597,6 +612,7 @@ cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
   a.staged = misses_staged ? 1 : 0;
   a.compact = L.compact ? 1 : 0;
   a.early = (early && !misses_staged) ? 1 : 0;
+  a.ready = p.scr.ready;
   const size_t smem = attn_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

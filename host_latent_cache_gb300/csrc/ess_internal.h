@@ -105,6 +105,9 @@ struct Scratch {
   uint16_t* h_qmla = nullptr;
   float* h_out = nullptr;
   int32_t* status = nullptr;      // device status word
+  // [B] CTAs of the selection (or the victim CTA, counting for all of them)
+  // done writing request b's lists; zeroed by the selection's first CTA
+  int32_t* ready = nullptr;
 };
 
 // Workspace layout computed from a config (offsets in bytes).
@@ -116,7 +119,7 @@ struct Layout {
       o_tail, o_guess;
   // scratch (absolute)
   size_t o_scores, o_tidx, o_tslot, o_nmw, o_mtok, o_mslot, o_nmiss, o_vict, o_hist, o_po, o_pml,
-      o_hq, o_hw, o_hqm, o_hout, o_status, o_fhist, o_tflag;
+      o_hq, o_hw, o_hqm, o_hout, o_status, o_fhist, o_tflag, o_ready;
   int nch = 0;                    // attention chunks per (request, way)
 };
 

@@ -46,11 +46,15 @@
 // Two kernels share this work: select_kernel produces everything the step
 // reads (the emitted lists, the miss union and its victims), and
 // lru_finish_kernel, which only the next step depends on, rewrites the state
-// and closes the next LRU list while the attention kernel runs.
+// and closes the next LRU list while the attention kernel runs.  Each
+// select_kernel CTA counts itself in a per-request counter once its share of
+// the lists is written, so a step's attention CTAs start on their own
+// request's lists without waiting for the slowest request.
 #include <algorithm>
 #include <mutex>
 
 #include "ess_device.cuh"
+#include "ess_sync.cuh"
 
 namespace ess {
 namespace {
@@ -94,6 +98,9 @@ struct SelArgs {
   int policy;                 // ESS_EVICT_*: LRU keeps the order list; the others
                               // leave the victims to victim_kernel
   unsigned long long seed;    // key of the Random victim order
+  // [B] or null: request b's lists are complete once this reaches kSelCluster
+  // (each selection CTA adds 1 under LRU; the victim CTA adds kSelCluster)
+  int* ready;
   // the layer's host rows, so that each miss's address translation starts
   // while the selection still runs (a prefetch; nothing waits for it)
   const uint8_t* host;        // device alias of the pinned host rows
@@ -362,6 +369,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   int parity = 0;
 
   if (tid == 0) {
+    // the previous step's readers of the counter completed before this grid
+    // passed its wait; this step's readers launch after the resolve below
+    if (a.ready != nullptr && rank == 0) atomicExch(a.ready + b, 0);
     sh.step_b = a.step[b];  // (also read directly as step0)
     sh.nl = 0;
     sh.fallback = 0;
@@ -1293,6 +1303,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   if (rank == 0 && tid == 0) {
     for (int m = 0; m < M; ++m) a.n_miss_way[b * M + m] = sh.nmw[m];
     a.n_miss[b] = n_miss_total;
+  }
+  if (lru && a.ready != nullptr) {
+    // this CTA's share of request b's lists is out
+    __syncthreads();
+    if (tid == 0) count_done(a.ready + b, 1);
+  }
+  if (rank == 0 && tid == 0) {
     if (a.stats) {
       long long h = 0, mi = 0;
       for (int m = 0; m < M; ++m) {
@@ -1346,8 +1363,11 @@ struct LruShared {
 
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
     lru_finish_kernel(const SelArgs a) {
-  pdl_wait_previous();
+  // whatever follows waits before it reads what the selection wrote: with
+  // griddepcontrol.wait, or (a step's attention) on the selection's counters,
+  // so it may launch before this grid's own wait is over
   pdl_launch_dependents();
+  pdl_wait_previous();
   extern __shared__ __align__(16) uint8_t dsm[];
   __shared__ LruShared sh;
   uint8_t* cflag = dsm;                                        // [c_local] stamped flags
@@ -1741,6 +1761,10 @@ __global__ void __launch_bounds__(kVicThreads, 1)
       a.topk_slot[wo + e] = ~vl[mi];
     }
   }
+  if (a.ready != nullptr) {
+    __syncthreads();
+    if (tid == 0) count_done(a.ready + b, kSelCluster);
+  }
 }
 
 __global__ void order_reset_kernel(int32_t* order, int n_per_list, int C) {
@@ -1842,6 +1866,7 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
   a.C = c.C;
   a.policy = p.evict_policy;
   a.seed = p.evict_seed;
+  a.ready = p.scr.ready;
   const SelSizes z = sel_sizes(c, L.T_hmax);
   a.n_local = z.nl;
   a.c_local = z.c_local;

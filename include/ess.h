@@ -299,9 +299,11 @@ ess_status ess_sparse_mla_decode(ess_pool* pool, int layer, const void* q_mla,
  *   ess_sparse_mla_decode.
  * Each kernel is launched as a programmatic dependent of the one before it on
  * the stream: its prologue overlaps the previous kernel, and it waits for that
- * kernel before touching memory.  With fused misses the attention kernel runs
- * beside the LRU finishing kernel (it reads only the lists the selection kernel
- * has already completed) and finishes only after it. */
+ * kernel before touching memory.  With fused misses the attention kernel may
+ * start while the selection still runs: each of its CTAs waits until the
+ * selection CTAs of its own request have counted themselves done in a
+ * per-request counter in the pool's scratch, then runs beside the LRU
+ * finishing kernel and finishes only after it. */
 ess_status ess_step(ess_pool* pool, int layer, const void* q_idx, const float* w,
                     const void* q_mla, float* out, ess_stream_t stream);
 
