@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "ess_internal.h"
+#include "ess_sync.cuh"
 
 namespace ess {
 namespace {
@@ -83,7 +84,8 @@ Layout compute_layout(const ess_config& c) {
   L.o_status = o;   o = align256(o + 256);
   L.o_fhist = o;    o = align256(o + B * M * kFineBins * 4);
   L.o_tflag = o;    o = align256(o + B * M * ((T + 31) / 32) * 4);
-  L.o_ready = o;    o = align256(o + B * 4);
+  L.o_ready = o;    o = align256(o + B * kCounterStride * 4);
+  L.o_adone = o;    o = align256(o + B * M * kCounterStride * 4);
   L.total = o;
   return L;
 }
@@ -280,6 +282,7 @@ ess_status ess_pool_create(const ess_config* cfg, void* dev_workspace, size_t ws
   r.fhist = reinterpret_cast<uint32_t*>(p->ws + L.o_fhist);
   r.tflag = reinterpret_cast<uint32_t*>(p->ws + L.o_tflag);
   r.ready = reinterpret_cast<int32_t*>(p->ws + L.o_ready);
+  r.attn_done = reinterpret_cast<int32_t*>(p->ws + L.o_adone);
   r.nwords = (cfg->max_T + 31) / 32;
   cudaError_t e = cudaSuccess;
   for (int l = 0; l < cfg->n_layers && e == cudaSuccess; ++l) {
@@ -288,7 +291,9 @@ ess_status ess_pool_create(const ess_config* cfg, void* dev_workspace, size_t ws
       e = cudaMemset(p->layers[l].pool, 0, static_cast<size_t>(cfg->batch) * cfg->C * kRowBytes);
   }
   if (e == cudaSuccess) e = cudaMemset(r.status, 0, 256);
-  if (e == cudaSuccess) e = cudaMemset(r.ready, 0, static_cast<size_t>(cfg->batch) * 4);
+  if (e == cudaSuccess)
+    e = cudaMemset(r.ready, 0, (L.o_adone - L.o_ready) + static_cast<size_t>(cfg->batch) *
+                                                           cfg->mtp * kCounterStride * 4);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     delete[] p->layers;

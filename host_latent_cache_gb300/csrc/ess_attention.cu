@@ -61,9 +61,11 @@ struct AttnArgs {
   // selection that wrote the lists read here.  The grid may launch while that
   // selection still runs: each CTA waits for its request's counter in ready
   // instead, and the wait for the finishing kernel moves to the end so the
-  // two run side by side
+  // two run side by side.  Each CTA then counts its partial out in
+  // attn_done, on which the merge kernel waits instead of this whole grid.
   int early;
   const int* ready;           // [B] completion counters of the selection (early only)
+  int* attn_done;             // [B][M] completion counters of this grid (early only)
 };
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -87,6 +89,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int c = blockIdx.x, m = blockIdx.y, b = blockIdx.z;
   const size_t wo = (static_cast<size_t>(b) * a.M + m) * a.k;
   const int qrow0 = (b * a.M + m) * a.H;
+  // early: the merge kernel waits on the counters, so it may launch as soon as
+  // every CTA of this grid is resident
+  if (a.early) pdl_launch_dependents();
 
   if (tid == 0) {
     for (int i = 0; i < QST; ++i) {
@@ -133,7 +138,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // this grid, launch).  Past the limit the chunk is treated as empty.
     __shared__ int lists_ok;
     if (tid == 0) {
-      lists_ok = wait_count(a.ready + b, kSelCluster) ? 1 : 0;
+      lists_ok = wait_count(a.ready + b * kCounterStride, kSelCluster) ? 1 : 0;
       if (!lists_ok) set_status(a.status, ESS_ERR_TIMEOUT);
     }
     __syncthreads();
@@ -396,9 +401,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   if (tid == 0) bulk_wait_all();
   if (a.early) pdl_wait_previous();   // finish only after the LRU finishing kernel
-  pdl_launch_dependents();
+  else pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
+  if (a.early && tid == 0) {
+    // the partial is out (the bulk copy complete, every (max, sum) written
+    // before the barrier) and the finishing kernel has completed: count it
+    fence_proxy_async_global();
+    count_done(a.attn_done + (b * a.M + m) * kCounterStride, 1);
+  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -410,16 +421,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // kMergeBatch chunks at a time, rescaling the running sums when M grows).  One
 // CTA per (head, request-way); thread t owns dims 4t..4t+3.  Launched as a
 // programmatic dependent of the attention kernel: it waits for that grid
-// before reading the partials.  Eight chunks' loads are in flight per thread
+// before reading the partials, or, inside a step (done given), only for the
+// counter of its own (request, way).  Eight chunks' loads are in flight per thread
 // (two rounds of L2 latency instead of four), with few enough registers that
 // every CTA is still resident beside the attention CTAs (a second wave would
 // add its whole latency to the step).
 __global__ void __launch_bounds__(128, kMergeMinBlocks) merge_kernel(const uint16_t* __restrict__ part_o,
                                                     const float2* __restrict__ part_ml,
-                                                    float* __restrict__ out, int H, int nch) {
-  pdl_wait_previous();
-  pdl_launch_dependents();
+                                                    float* __restrict__ out, int H, int nch,
+                                                    const int* done, int* status) {
   const int h = blockIdx.x, bm = blockIdx.y, t = threadIdx.x;
+  if (done != nullptr) {
+    // the nch chunk CTAs of (request, way) bm count themselves once their
+    // partials are out; the attention CTAs are all resident before this grid
+    // launches.  Past the limit the error is recorded and the merge goes on.
+    if (t == 0 && !wait_count(done + bm * kCounterStride, nch)) set_status(status, ESS_ERR_TIMEOUT);
+    __syncthreads();
+  } else {
+    pdl_wait_previous();
+  }
+  pdl_launch_dependents();
   const float2* ml = part_ml + static_cast<size_t>(bm) * nch * H + h;
   // dims 4t..4t+3 of head h: half of the 16-byte unit t/2, stored at unit (t/2) ^ (h & 7)
   const int u = (t >> 1) ^ (h & 7);
@@ -434,8 +455,8 @@ __global__ void __launch_bounds__(128, kMergeMinBlocks) merge_kernel(const uint1
 #pragma unroll
     for (int q = 0; q < kMergeBatch; ++q) {
       const int c = c0 + q;
-      e[q] = c < nch ? __ldg(ml + static_cast<size_t>(c) * H) : make_float2(-INFINITY, 0.0f);
-      v[q] = c < nch ? __ldg(po + static_cast<size_t>(c) * cstride) : make_uint2(0u, 0u);
+      e[q] = c < nch ? __ldcg(ml + static_cast<size_t>(c) * H) : make_float2(-INFINITY, 0.0f);
+      v[q] = c < nch ? __ldcg(po + static_cast<size_t>(c) * cstride) : make_uint2(0u, 0u);
     }
     float Mg = M;
 #pragma unroll
@@ -613,6 +634,7 @@ cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
   a.compact = L.compact ? 1 : 0;
   a.early = (early && !misses_staged) ? 1 : 0;
   a.ready = p.scr.ready;
+  a.attn_done = p.scr.attn_done;
   const size_t smem = attn_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -623,7 +645,8 @@ cudaError_t launch_attention(const ess_pool& p, int layer, const void* q_mla,
   count_launch(p);
   e = launch_pdl(merge_kernel, dim3(c.mla_heads, c.batch * c.mtp), dim3(128), 0, st,
                  static_cast<const uint16_t*>(p.scr.part_o), static_cast<const float2*>(p.scr.part_ml),
-                 out, c.mla_heads, a.nch);
+                 out, c.mla_heads, a.nch,
+                 static_cast<const int*>(a.early ? p.scr.attn_done : nullptr), p.scr.status);
   if (e == cudaSuccess) count_launch(p);
   return e;
 }

@@ -105,9 +105,12 @@ struct Scratch {
   uint16_t* h_qmla = nullptr;
   float* h_out = nullptr;
   int32_t* status = nullptr;      // device status word
-  // [B] CTAs of the selection (or the victim CTA, counting for all of them)
-  // done writing request b's lists; zeroed by the selection's first CTA
+  // completion counters, one 128-byte line apart, zeroed by the first
+  // selection CTA of their request: [B] selection CTAs (or the victim CTA,
+  // counting for all of them) done writing request b's lists; [B][M]
+  // attention CTAs done writing the partials of (request b, way m)
   int32_t* ready = nullptr;
+  int32_t* attn_done = nullptr;
 };
 
 // Workspace layout computed from a config (offsets in bytes).
@@ -119,7 +122,7 @@ struct Layout {
       o_tail, o_guess;
   // scratch (absolute)
   size_t o_scores, o_tidx, o_tslot, o_nmw, o_mtok, o_mslot, o_nmiss, o_vict, o_hist, o_po, o_pml,
-      o_hq, o_hw, o_hqm, o_hout, o_status, o_fhist, o_tflag, o_ready;
+      o_hq, o_hw, o_hqm, o_hout, o_status, o_fhist, o_tflag, o_ready, o_adone;
   int nch = 0;                    // attention chunks per (request, way)
 };
 

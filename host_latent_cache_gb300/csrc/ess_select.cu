@@ -98,9 +98,12 @@ struct SelArgs {
   int policy;                 // ESS_EVICT_*: LRU keeps the order list; the others
                               // leave the victims to victim_kernel
   unsigned long long seed;    // key of the Random victim order
-  // [B] or null: request b's lists are complete once this reaches kSelCluster
-  // (each selection CTA adds 1 under LRU; the victim CTA adds kSelCluster)
+  // [B] counters or null: request b's lists are complete once its counter
+  // reaches kSelCluster (each selection CTA adds 1 under LRU; the victim CTA
+  // adds kSelCluster); [B][M] counters of the attention kernel's chunk CTAs.
+  // Both are zeroed by the request's first CTA.
   int* ready;
+  int* attn_done;
   // the layer's host rows, so that each miss's address translation starts
   // while the selection still runs (a prefetch; nothing waits for it)
   const uint8_t* host;        // device alias of the pinned host rows
@@ -371,7 +374,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   if (tid == 0) {
     // the previous step's readers of the counter completed before this grid
     // passed its wait; this step's readers launch after the resolve below
-    if (a.ready != nullptr && rank == 0) atomicExch(a.ready + b, 0);
+    if (a.ready != nullptr && rank == 0) {
+      atomicExch(a.ready + b * kCounterStride, 0);
+      for (int m = 0; m < M; ++m) atomicExch(a.attn_done + (b * M + m) * kCounterStride, 0);
+    }
     sh.step_b = a.step[b];  // (also read directly as step0)
     sh.nl = 0;
     sh.fallback = 0;
@@ -1307,7 +1313,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1)
   if (lru && a.ready != nullptr) {
     // this CTA's share of request b's lists is out
     __syncthreads();
-    if (tid == 0) count_done(a.ready + b, 1);
+    if (tid == 0) count_done(a.ready + b * kCounterStride, 1);
   }
   if (rank == 0 && tid == 0) {
     if (a.stats) {
@@ -1763,7 +1769,7 @@ __global__ void __launch_bounds__(kVicThreads, 1)
   }
   if (a.ready != nullptr) {
     __syncthreads();
-    if (tid == 0) count_done(a.ready + b, kSelCluster);
+    if (tid == 0) count_done(a.ready + b * kCounterStride, kSelCluster);
   }
 }
 
@@ -1867,6 +1873,7 @@ cudaError_t launch_select(const ess_pool& p, int layer, const float* scores, boo
   a.policy = p.evict_policy;
   a.seed = p.evict_seed;
   a.ready = p.scr.ready;
+  a.attn_done = p.scr.attn_done;
   const SelSizes z = sel_sizes(c, L.T_hmax);
   a.n_local = z.nl;
   a.c_local = z.c_local;
